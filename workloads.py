@@ -1,0 +1,182 @@
+"""Seeded synthetic inputs for sparse MLA attention over a paged KV cache.
+
+This module only draws inputs; it contains none of the attention arithmetic.
+Both the oracle (``oracle/``) and the CUDA path receive exactly the arrays
+built here, generated on the CPU with ``torch.Generator().manual_seed(seed)``
+and handed over as numpy arrays (bf16 values as their uint16 bit patterns).
+
+Layouts (row-major, the operator's I/O table):
+  q_nope  (B*S1, n_q, 512) bf16      q_rope (B*S1, n_q, 64) bf16
+  kv_nope (num_blocks*128, 512) bf16 | int8
+  kv_rope (num_blocks*128, 64) bf16  kv_scales (num_blocks*128, 4) fp32 (INT8 only)
+  topk_idx (B*S1, topk) int32        block_table (B, max_blocks_per_seq) int32
+  act_seqs (B,) int32
+
+The five named workloads follow the shapes of the pages' test cases and timing
+table (B=64, S1=2, S2=8192, D=512; act_seq up to 65536; a prefill run) with
+q/k drawn from N(0, 1).  No public dataset is involved.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+D_NOPE = 512
+D_ROPE = 64
+BLOCK_SIZE = 128
+BF16_NAN_BITS = 0x7FC0
+
+
+def _bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.to(torch.bfloat16).contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _randn_bf16(g: torch.Generator, shape, chunk_rows: int = 1 << 16) -> np.ndarray:
+    """N(0, 1) rounded to bf16, drawn in row chunks to bound peak memory."""
+    rows = shape[0]
+    out = np.empty(shape, dtype=np.uint16)
+    for r0 in range(0, rows, chunk_rows):
+        r1 = min(rows, r0 + chunk_rows)
+        out[r0:r1] = _bf16_bits(torch.randn((r1 - r0,) + tuple(shape[1:]), generator=g))
+    return out
+
+
+def quantize_int8_groups(x: torch.Tensor):
+    """Per-row INT8 with one fp32 scale per 128-element group.
+
+    scale = absmax / 127 (a group of zeros gets scale 1), q = clamp(round(x / scale),
+    -128, 127) with round-half-to-even.  This is how the synthetic INT8 cache is
+    written; the attention path only ever reads q and scale back.
+    """
+    rows, d = x.shape
+    grp = x.reshape(rows, d // 128, 128)
+    absmax = grp.abs().amax(dim=-1)
+    scale = absmax / 127.0
+    scale = torch.where(absmax > 0, scale, torch.ones_like(scale))
+    q = torch.round(grp / scale[..., None]).clamp_(-128, 127).to(torch.int8)
+    return q.reshape(rows, d).numpy(), scale.to(torch.float32).numpy()
+
+
+def make_inputs(*, B: int, S1: int, n_q: int, act_seqs, topk: int, seed: int, num_blocks: int | None = None,
+                max_blocks_per_seq: int | None = None, kv_int8: bool = False, positions=None,
+                poison_unused: bool = True, softmax_scale: float | None = None, mode: str = "decode",
+                name: str = "custom") -> dict:
+    """Build one workload.
+
+    act_seqs: per-batch actual KV length.  Each batch gets ceil(act/128)
+    physical blocks, drawn without replacement from a random permutation of
+    ``num_blocks`` (default: exactly the blocks needed); the table is padded
+    with -1.  ``positions`` (optional, (B, S1)) gives each token's position p:
+    the token then selects among [0, p] (causal prefill); otherwise among
+    [0, act).  A token selects min(topk, n) distinct indices uniformly (n =
+    its candidate count) in random order, padded with -1.  Cache rows that no
+    valid index can reach (unused blocks, positions >= act) are NaN when
+    ``poison_unused``.
+    """
+    g = torch.Generator().manual_seed(int(seed))
+    act = np.asarray(act_seqs, dtype=np.int64).reshape(B)
+    nb = [(int(a) + BLOCK_SIZE - 1) // BLOCK_SIZE for a in act]
+    used = int(sum(nb))
+    if num_blocks is None:
+        num_blocks = max(used, 1)
+    if num_blocks < used:
+        raise ValueError("num_blocks smaller than the blocks the sequences need")
+    if max_blocks_per_seq is None:
+        max_blocks_per_seq = max(max(nb), 1)
+    perm = torch.randperm(num_blocks, generator=g).numpy().astype(np.int32)
+    block_table = np.full((B, max_blocks_per_seq), -1, dtype=np.int32)
+    o = 0
+    for b in range(B):
+        block_table[b, : nb[b]] = perm[o:o + nb[b]]
+        o += nb[b]
+    T = B * S1
+    topk_idx = np.full((T, topk), -1, dtype=np.int32)
+    for t in range(T):
+        b = t // S1
+        n_cand = int(act[b]) if positions is None else int(np.asarray(positions)[b, t % S1]) + 1
+        n_cand = max(0, min(n_cand, int(act[b])))
+        k = min(topk, n_cand)
+        if k > 0:
+            topk_idx[t, :k] = torch.randperm(n_cand, generator=g)[:k].numpy().astype(np.int32)
+    rows = num_blocks * BLOCK_SIZE
+    if kv_int8:
+        kv_nope = np.empty((rows, D_NOPE), dtype=np.int8)
+        kv_scales = np.empty((rows, D_NOPE // 128), dtype=np.float32)
+        step = 1 << 15
+        for r0 in range(0, rows, step):
+            r1 = min(rows, r0 + step)
+            q8, sc = quantize_int8_groups(torch.randn((r1 - r0, D_NOPE), generator=g))
+            kv_nope[r0:r1] = q8
+            kv_scales[r0:r1] = sc
+    else:
+        kv_nope = _randn_bf16(g, (rows, D_NOPE))
+        kv_scales = None
+    kv_rope = _randn_bf16(g, (rows, D_ROPE))
+    q_nope = _randn_bf16(g, (T, n_q, D_NOPE))
+    q_rope = _randn_bf16(g, (T, n_q, D_ROPE))
+    if poison_unused:
+        reach = np.zeros(rows, dtype=bool)
+        for b in range(B):
+            for s in range(nb[b]):
+                blk = block_table[b, s]
+                lo = blk * BLOCK_SIZE
+                n_valid = min(BLOCK_SIZE, int(act[b]) - s * BLOCK_SIZE)
+                reach[lo:lo + n_valid] = True
+        dead = ~reach
+        if dead.any():
+            kv_rope[dead] = BF16_NAN_BITS
+            if kv_int8:
+                kv_scales[dead] = np.nan
+            else:
+                kv_nope[dead] = BF16_NAN_BITS
+    dims = dict(B=B, S1=S1, n_q=n_q, n_kv=1, d_nope=D_NOPE, d_rope=D_ROPE, block_size=BLOCK_SIZE,
+                num_blocks=int(num_blocks), max_blocks_per_seq=int(max_blocks_per_seq), topk=int(topk),
+                kv_int8=int(bool(kv_int8)))
+    return dict(name=name, dims=dims, q_nope=q_nope, q_rope=q_rope, kv_nope=kv_nope, kv_rope=kv_rope,
+                kv_scales=kv_scales, topk_idx=topk_idx, block_table=block_table,
+                act_seqs=act.astype(np.int32),
+                softmax_scale=float(softmax_scale if softmax_scale is not None else 1.0 / math.sqrt(D_NOPE + D_ROPE)),
+                mode=mode)
+
+
+# ------------------------------------------------------------------ named workloads
+def tiny_decode(seed: int = 0) -> dict:
+    """B=1 S1=1 H=16, act 256 over 2 of 4 physical blocks (2 NaN-filled), topk 64."""
+    return make_inputs(B=1, S1=1, n_q=16, act_seqs=[256], topk=64, num_blocks=4, seed=seed, name="tiny_decode")
+
+
+def mtp_decode(seed: int = 1, B: int = 64) -> dict:
+    """B=64 S1=2 H=128, act 8192 each, 4096 shuffled blocks, topk 2048 distinct, bf16."""
+    return make_inputs(B=B, S1=2, n_q=128, act_seqs=[8192] * B, topk=2048, seed=seed, name="mtp_decode")
+
+
+def int8_decode(seed: int = 2, B: int = 64) -> dict:
+    """As mtp_decode with key_nope INT8 per 128-group (scale = absmax/127)."""
+    return make_inputs(B=B, S1=2, n_q=128, act_seqs=[8192] * B, topk=2048, seed=seed, kv_int8=True,
+                       name="int8_decode")
+
+
+def varlen_decode(seed: int = 3, B: int = 64) -> dict:
+    """B=64 S1=2 H=128 topk 2048, act_b ~ U{512..65536}, shuffled blocks, -1 padding."""
+    g = torch.Generator().manual_seed(int(seed) + 1000)
+    act = torch.randint(512, 65537, (B,), generator=g).numpy()
+    return make_inputs(B=B, S1=2, n_q=128, act_seqs=act, topk=2048, seed=seed, name="varlen_decode")
+
+
+def prefill(seed: int = 4, B: int = 4, S1: int = 1024) -> dict:
+    """B=4, S1=1024 tokens at positions 7168..8191 of act 8192, causal top-2048."""
+    act = 8192
+    pos = np.tile(np.arange(act - S1, act, dtype=np.int64), (B, 1))
+    return make_inputs(B=B, S1=S1, n_q=128, act_seqs=[act] * B, topk=2048, seed=seed, positions=pos,
+                       mode="prefill", name="prefill")
+
+
+NAMED = {
+    "tiny_decode": tiny_decode,
+    "mtp_decode": mtp_decode,
+    "int8_decode": int8_decode,
+    "varlen_decode": varlen_decode,
+    "prefill": prefill,
+}

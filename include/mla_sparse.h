@@ -1,0 +1,141 @@
+/*
+ * mla_sparse.h -- C ABI of the GB300 (sm_103a) sparse MLA attention library.
+ *
+ * Operation (sparse_flash_attention_quant, "DeepSeek V3/V2 Sparse Flash
+ * Attention with Quantization": sections "Algorithm overview", "Operator
+ * spec", "Inputs / outputs", "Compute pipeline" and "INT8 quantization path";
+ * the selection rule is o_i = Attn(x_i, {c_j : j in Top-k(I_i,:)}) from "CANN
+ * DeepSeek Indexer attention", section "Sparse Flash Attention"):
+ *
+ *   for every query token t = (b, s) and query head h (all heads share the one
+ *   latent KV head, N_KV = 1):
+ *     valid entries  i : 0 <= topk_idx[t, i] < act_seqs[b]
+ *     row            r_i = block_table[b, j / 128] * 128 + j % 128, j = topk_idx[t, i]
+ *     score          z_i = softmax_scale * (q_nope[t,h,:] . kv_nope[r_i,:]
+ *                                         + q_rope[t,h,:] . kv_rope[r_i,:])
+ *     out[t,h,:]   = sum_i softmax(z)_i * kv_nope[r_i,:]      (value = key_nope)
+ *     lse[t,h]     = ln sum_i exp(z_i)
+ *   INT8 cache rows are dequantised per 128-element group as
+ *   bf16(fp32(q8) * scale) before use.  A token with no valid entry gets
+ *   out = 0 and lse = -inf.  Repeated indices count once per occurrence.
+ *
+ * Conventions
+ *   - Every data pointer is a DEVICE pointer owned by the caller; the library
+ *     allocates nothing and keeps no state besides a sticky device status word.
+ *   - All tensors are dense row-major with the shapes given below.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream) and never synchronise.
+ *   - Argument errors are detected on the host before any launch and return a
+ *     negative status; mla_sparse_last_error() then describes the problem
+ *     (thread-local, valid until the next call on the same thread).
+ *   - Bad block ids for valid indices (outside [0, num_blocks), or a table
+ *     slot index / 128 beyond max_blocks_per_seq) never fault: the entry is
+ *     masked out of the softmax and MLA_DEVICE_BAD_BLOCK is raised in the
+ *     device status word.  Every internal wait of the kernel is bounded; a
+ *     wait that runs out raises MLA_DEVICE_TIMEOUT (sticky: later launches do
+ *     no work until the status is cleared).
+ *   - Numerics: inputs bf16; products are exact; score and output
+ *     accumulation in fp32 on the tensor cores; the softmax weights P and the
+ *     values enter the P.V product as fp16 (exact conversion of bf16 values
+ *     whose magnitude lies in [2^-14, 65504]); out is rounded to bf16 once.
+ */
+#ifndef MLA_SPARSE_H_
+#define MLA_SPARSE_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mla_status {
+  MLA_OK = 0,
+  MLA_ERR_NULL = -1,           /* a required pointer is NULL */
+  MLA_ERR_SHAPE = -2,          /* a dimension is out of range */
+  MLA_ERR_DTYPE = -3,          /* kv_dtype unknown, or scales missing for INT8 */
+  MLA_ERR_UNSUPPORTED = -4,    /* a valid but unimplemented configuration */
+  MLA_ERR_ALIGN = -5,          /* a pointer is not aligned as required */
+  MLA_ERR_CUDA = -6,           /* the CUDA runtime reported an error */
+  MLA_ERR_DEVICE_STATUS = -7   /* the device status word holds an error */
+} mla_status;
+
+typedef enum mla_mode {
+  MLA_MODE_DECODE = 0,   /* "Decode mode": standard softmax over the token's selection */
+  MLA_MODE_PREFILL = 1   /* "Prefill mode": flash online softmax across key tiles */
+} mla_mode;
+
+typedef enum mla_kv_dtype {
+  MLA_KV_BF16 = 0,   /* kv_nope holds bf16 */
+  MLA_KV_INT8 = 1    /* kv_nope holds int8 with one fp32 scale per 128 elements */
+} mla_kv_dtype;
+
+/* Device status bits (mla_sparse_device_status). */
+#define MLA_DEVICE_BAD_BLOCK 0x1u
+#define MLA_DEVICE_TIMEOUT 0x2u
+
+/*
+ * Problem dimensions ("Inputs / outputs" table).  Supported today:
+ * n_kv == 1, d_nope == 512 (kv_lora_rank), d_rope == 64 (qk_rope_dim),
+ * block_size == 128, 1 <= n_q <= 128, topk >= 1, num_blocks in [1, 2^24).
+ */
+typedef struct mla_dims {
+  int32_t B;                  /* batch */
+  int32_t S1;                 /* query tokens per batch entry */
+  int32_t n_q;                /* query heads N_Q */
+  int32_t n_kv;               /* latent KV heads N_KV */
+  int32_t d_nope;             /* kv_lora_rank */
+  int32_t d_rope;             /* qk_rope_dim */
+  int32_t block_size;         /* paged-cache block size */
+  int32_t num_blocks;         /* physical blocks in the cache */
+  int32_t max_blocks_per_seq; /* width of block_table */
+  int32_t topk;               /* entries per token in topk_idx */
+  int32_t kv_dtype;           /* mla_kv_dtype */
+} mla_dims;
+
+/*
+ * mla_sparse_attn_fwd -- sparse MLA attention forward over a paged cache.
+ *
+ *   q_nope      bf16 [B*S1, n_q, d_nope]                       16-byte aligned
+ *   q_rope      bf16 [B*S1, n_q, d_rope]                       16-byte aligned
+ *   kv_nope     bf16 | int8 [num_blocks*block_size, d_nope]    16-byte aligned
+ *   kv_rope     bf16 [num_blocks*block_size, d_rope]           16-byte aligned
+ *   kv_scales   fp32 [num_blocks*block_size, d_nope/128]; required (16-byte
+ *               aligned) for MLA_KV_INT8, ignored for MLA_KV_BF16
+ *   topk_idx    int32 [B*S1, n_kv*topk]: logical positions; entries < 0 or
+ *               >= act_seqs[b] are masked
+ *   block_table int32 [B, max_blocks_per_seq]: physical block of each logical block
+ *   act_seqs    int32 [B]: actual KV length of each batch entry
+ *   out         bf16 [B, S1, n_q, d_nope] (written)                16-byte aligned
+ *   lse         fp32 [B, S1, n_q] (written) or NULL
+ *   softmax_scale  finite scale applied to the summed nope + rope score
+ *   mode        mla_mode: selects the schedule only; both modes compute the
+ *               same function
+ *   stream      cudaStream_t
+ *
+ * Returns MLA_OK once the work is enqueued, or a negative mla_status.
+ */
+mla_status mla_sparse_attn_fwd(const mla_dims* dims, const void* q_nope, const void* q_rope,
+                               const void* kv_nope, const void* kv_rope, const float* kv_scales,
+                               const int32_t* topk_idx, const int32_t* block_table,
+                               const int32_t* act_seqs, void* out, float* lse, float softmax_scale,
+                               int32_t mode, void* stream);
+
+/* Description of the last error on this thread ("" after a success). */
+const char* mla_sparse_last_error(void);
+
+/*
+ * Synchronises `stream`, reads the device status word of the current device
+ * into *flags (MLA_DEVICE_* bits; flags may be NULL) and clears it when
+ * `clear` is non-zero.  Returns MLA_ERR_DEVICE_STATUS if any bit was set,
+ * MLA_ERR_CUDA on a runtime error, MLA_OK otherwise.
+ */
+mla_status mla_sparse_device_status(void* stream, uint32_t* flags, int32_t clear);
+
+/* ABI version of this header (major * 100 + minor). */
+int32_t mla_sparse_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_SPARSE_H_ */

@@ -1,0 +1,129 @@
+"""ctypes binding of the C ABI in include/mla_sparse.h.
+
+Argument marshalling only: shapes and dtypes are read off torch tensors, the
+device pointers and the current CUDA stream are passed through, and a
+negative status becomes an exception.  Every step of the computation runs in
+the CUDA library; there is no other implementation to fall back to, and a
+missing library is an error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmla_sparse.so")
+
+MLA_OK = 0
+MLA_MODE_DECODE = 0
+MLA_MODE_PREFILL = 1
+MLA_KV_BF16 = 0
+MLA_KV_INT8 = 1
+MLA_DEVICE_BAD_BLOCK = 0x1
+MLA_DEVICE_TIMEOUT = 0x2
+
+EXPORTED_SYMBOLS = ("mla_sparse_attn_fwd", "mla_sparse_last_error", "mla_sparse_device_status",
+                    "mla_sparse_abi_version")
+
+
+class MlaDims(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_int32) for name in (
+        "B", "S1", "n_q", "n_kv", "d_nope", "d_rope", "block_size", "num_blocks", "max_blocks_per_seq",
+        "topk", "kv_dtype")]
+
+
+class MlaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"mla_sparse status {status}: {message}")
+        self.status = status
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it first (python -m mla_sparse_top_gb300.build)")
+    lib = ctypes.CDLL(path)
+    vp = ctypes.c_void_p
+    lib.mla_sparse_attn_fwd.argtypes = [ctypes.POINTER(MlaDims)] + [vp] * 10 + [ctypes.c_float, ctypes.c_int32, vp]
+    lib.mla_sparse_attn_fwd.restype = ctypes.c_int
+    lib.mla_sparse_last_error.argtypes = []
+    lib.mla_sparse_last_error.restype = ctypes.c_char_p
+    lib.mla_sparse_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int32]
+    lib.mla_sparse_device_status.restype = ctypes.c_int
+    lib.mla_sparse_abi_version.argtypes = []
+    lib.mla_sparse_abi_version.restype = ctypes.c_int32
+    _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != MLA_OK:
+        raise MlaError(status, load_library().mla_sparse_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def make_dims(q_nope, kv_nope, topk_idx, block_table, kv_int8: bool, S1: int) -> MlaDims:
+    T, n_q, d_nope = q_nope.shape
+    if T % S1:
+        raise ValueError("q_nope's leading dim must be B*S1")
+    rows = kv_nope.shape[0]
+    return MlaDims(B=T // S1, S1=S1, n_q=n_q, n_kv=1, d_nope=d_nope, d_rope=64, block_size=128,
+                   num_blocks=rows // 128, max_blocks_per_seq=block_table.shape[1], topk=topk_idx.shape[1],
+                   kv_dtype=MLA_KV_INT8 if kv_int8 else MLA_KV_BF16)
+
+
+def mla_sparse_attn_fwd(q_nope, q_rope, kv_nope, kv_rope, kv_scales, topk_idx, block_table, act_seqs, out,
+                        lse=None, softmax_scale=None, mode: int | str = MLA_MODE_DECODE, S1: int = 1,
+                        stream=None, dims: MlaDims | None = None):
+    """Enqueue one call of the C entry point with the same name.
+
+    q_nope (B*S1, n_q, 512) bf16, q_rope (B*S1, n_q, 64) bf16, kv_nope
+    (rows, 512) bf16|int8, kv_rope (rows, 64) bf16, kv_scales (rows, 4) fp32 or
+    None, topk_idx (B*S1, topk) int32, block_table (B, W) int32, act_seqs (B,)
+    int32, out (B*S1, n_q, 512) bf16, lse (B*S1, n_q) fp32 or None.
+    """
+    lib = load_library()
+    kv_int8 = kv_nope.dtype == torch.int8
+    if dims is None:
+        dims = make_dims(q_nope, kv_nope, topk_idx, block_table, kv_int8, S1)
+    if isinstance(mode, str):
+        mode = {"decode": MLA_MODE_DECODE, "prefill": MLA_MODE_PREFILL}[mode]
+    if softmax_scale is None:
+        softmax_scale = (dims.d_nope + dims.d_rope) ** -0.5
+    st = lib.mla_sparse_attn_fwd(ctypes.byref(dims), _ptr(q_nope), _ptr(q_rope), _ptr(kv_nope), _ptr(kv_rope),
+                                 _ptr(kv_scales if kv_int8 else None), _ptr(topk_idx), _ptr(block_table),
+                                 _ptr(act_seqs), _ptr(out), _ptr(lse), ctypes.c_float(softmax_scale),
+                                 ctypes.c_int32(int(mode)), _stream_handle(stream))
+    _check(st)
+    return out, lse
+
+
+def device_status(clear: bool = True, stream=None) -> int:
+    """Synchronise the stream and return (and by default clear) the status bits."""
+    lib = load_library()
+    flags = ctypes.c_uint32(0)
+    st = lib.mla_sparse_device_status(_stream_handle(stream), ctypes.byref(flags), 1 if clear else 0)
+    if st not in (MLA_OK, -7):
+        _check(st)
+    return int(flags.value)
+
+
+def abi_version() -> int:
+    return int(load_library().mla_sparse_abi_version())

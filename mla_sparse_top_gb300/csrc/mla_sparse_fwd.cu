@@ -1,0 +1,697 @@
+// Fused sparse MLA attention forward for GB300 (sm_103a).
+//
+// One query token is processed by a cluster of two CTAs.  CTA r (its rank in
+// the cluster) owns the latent dims [256r, 256r+256) and the rope dims
+// [32r, 32r+32): it gathers only that half of every selected cache row, so no
+// byte is read twice, and it accumulates O[:, its 256 dims] for all 128 heads
+// in tensor memory.  Scores need all 576 dims, so each CTA computes a partial
+// score tile over its half and the two partials are exchanged through
+// distributed shared memory (st.async + mbarrier transaction counts); both
+// CTAs then hold the same full score tile and run the same online softmax.
+//
+// Per CTA (448 threads):
+//   warps 0-3   softmax: TMEM lane h = head h.  Load Q (latent part into TMEM,
+//               rope part into shared memory), per key tile read S, exchange
+//               with the peer, mask/scale/online softmax, write P into TMEM as
+//               two bf16 terms P_hi = bf16(p), P_lo = bf16(p - P_hi), rescale
+//               O when the running max grows by more than 2^8, final O / l ->
+//               bf16 and lse.
+//   warps 4-11  gather: two groups of four warps, alternating key tiles; for
+//               each selected row copy the half row into the 128-byte-swizzled
+//               layout of the stage ring (bf16: cp.async with zero fill for
+//               masked entries; int8: load, dequantise to bf16, store).
+//   warp 12     MMA issue (one thread): S = Q.K^T (A = Q in TMEM / smem, B = K
+//               tile, K-major) and O += P_hi.V + P_lo.V (A = P in TMEM, B = V
+//               tile, MN-major), tcgen05 bf16 with FP32 accumulators in TMEM.
+//
+// Precision: every product is exact (bf16 x bf16 into fp32).  Splitting P in
+// two bf16 terms keeps its relative error below 2^-18, so the result stays
+// within the stated tolerance of the exact definition even when few keys
+// carry the weight (P rounded once to bf16 or fp16 does not).
+//   warp 13     index resolution, up to eight tiles ahead: topk entry ->
+//               validity -> block_table -> physical row.
+//
+// The stages of the computation follow "DeepSeek V3/V2 Sparse Flash Attention
+// with Quantization", section "Compute pipeline": Sa_V0 gather (+ INT8
+// dequant), Sa_C1 S = Q K^T, Sa_V1 softmax(S * scale), Sa_C2 O = P V, Sa_V2
+// O = o / l on the last tile; the running (m, l, o) update is the one of the
+// section "Flash online softmax incremental update".
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/mla_sparse.h"
+#include "ptx.cuh"
+
+namespace mlasp {
+
+// ------------------------------------------------------------------ layout
+constexpr int kThreads = 448;
+constexpr int kGatherWarp0 = 4;
+constexpr int kMmaWarp = 12;
+constexpr int kTileKeys = 64;
+constexpr int kStages = 4;
+constexpr int kIdxSlots = 8;
+constexpr int kHeads = 128;
+constexpr int kChunkBytes = kTileKeys * 128;   // 64 keys x 64 bf16 dims
+constexpr int kStageBytes = 5 * kChunkBytes;   // 4 latent chunks + 1 rope chunk
+constexpr int kRecvBytes = kHeads * kTileKeys * 4;
+
+constexpr int kQRopeBytes = kHeads * 128;     // Q rope half, 128-byte rows (64 B used)
+
+constexpr int kOffStages = 0;
+constexpr int kOffRecv = kOffStages + kStages * kStageBytes;
+constexpr int kOffQRope = kOffRecv + kRecvBytes;
+constexpr int kOffRows = kOffQRope + kQRopeBytes;                // int32 [kIdxSlots][64]
+constexpr int kOffVmask = kOffRows + kIdxSlots * kTileKeys * 4;  // uint16 [kStages][4]
+constexpr int kOffBars = kOffVmask + kStages * 4 * 2;
+// barrier indices
+constexpr int kBarFull = 0;                      // [kStages]
+constexpr int kBarEmpty = kBarFull + kStages;    // [kStages]
+constexpr int kBarIdxFull = kBarEmpty + kStages; // [kIdxSlots]
+constexpr int kBarIdxEmpty = kBarIdxFull + kIdxSlots;
+constexpr int kBarSFull = kBarIdxEmpty + kIdxSlots;
+constexpr int kBarSFree = kBarSFull + 1;
+constexpr int kBarPFull = kBarSFree + 1;
+constexpr int kBarPvDone = kBarPFull + 1;
+constexpr int kBarRecvFull = kBarPvDone + 1;
+constexpr int kBarPeerFree = kBarRecvFull + 1;
+constexpr int kBarQReady = kBarPeerFree + 1;
+constexpr int kBarFinal = kBarQReady + 1;
+constexpr int kNumBars = kBarFinal + 1;
+constexpr int kOffTmemSlot = kOffBars + kNumBars * 8;
+constexpr int kOffAbort = kOffTmemSlot + 4;
+constexpr int kSmemUsed = kOffAbort + 4;
+constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
+
+// TMEM columns (512 allocated): O | S | P_hi | P_lo | Q latent (bf16 pairs)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemO = 0;
+constexpr uint32_t kTmemS = 256;
+constexpr uint32_t kTmemPhi = 320;
+constexpr uint32_t kTmemPlo = 352;
+constexpr uint32_t kTmemQ = 384;
+static_assert(kTmemQ + 128 <= kTmemCols, "TMEM budget");
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;
+
+__device__ unsigned int g_mla_status = 0;
+
+struct Params {
+  const uint16_t* q_nope;
+  const uint16_t* q_rope;
+  const void* kv_nope;
+  const uint16_t* kv_rope;
+  const float* kv_scales;
+  const int32_t* topk_idx;
+  const int32_t* block_table;
+  const int32_t* act_seqs;
+  uint16_t* out;
+  float* lse;
+  int S1, n_q, topk, num_blocks, mbps, n_tiles;
+  float scale_log2;
+};
+
+struct Ctx {
+  uint32_t sbase;    // shared address of the aligned dynamic smem
+  uint8_t* smem;     // generic pointer to the same
+  uint32_t tmem;     // TMEM base
+  uint32_t crank;    // rank in the cluster (0/1)
+  int t;             // query token
+  volatile uint32_t* abort;
+  __device__ uint32_t bar(int i) const { return sbase + kOffBars + 8 * i; }
+};
+
+__device__ __forceinline__ bool wait_bar(const Ctx& c, int idx, uint32_t parity) {
+  return mbar_wait<false>(c.bar(idx), parity, c.abort, kWaitLimitNs);
+}
+// Warp-uniform variants: every lane waits (bounded) and the warp agrees on
+// the outcome, so warp-collective instructions after it never see a
+// partially departed warp.
+__device__ __forceinline__ bool warp_wait(const Ctx& c, int idx, uint32_t parity) {
+  return __all_sync(0xffffffffu, wait_bar(c, idx, parity));
+}
+__device__ __forceinline__ bool warp_wait_cluster(const Ctx& c, int idx, uint32_t parity) {
+  return __all_sync(0xffffffffu, mbar_wait<true>(c.bar(idx), parity, c.abort, kWaitLimitNs));
+}
+
+__device__ __forceinline__ uint4 ldg16(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+
+__device__ __forceinline__ void sts16(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ float4 lds16f(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// ------------------------------------------------------------------ index warp
+// Resolves topk entries of tiles [j0, j0+4) into physical row ids (-1: masked).
+__device__ void index_role(const Params& p, const Ctx& c, int lane) {
+  const int b = c.t / p.S1;
+  const int act = __ldg(p.act_seqs + b);
+  const int32_t* tk = p.topk_idx + static_cast<int64_t>(c.t) * p.topk;
+  const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.mbps;
+  int32_t* rows = reinterpret_cast<int32_t*>(c.smem + kOffRows);
+  bool bad = false;
+  for (int j0 = 0; j0 < p.n_tiles; j0 += 4) {
+    const int nb = min(4, p.n_tiles - j0);
+    bool ok = true;
+    for (int k = 0; k < nb && ok; ++k) {
+      const int j = j0 + k;
+      ok = warp_wait(c, kBarIdxEmpty + (j & (kIdxSlots - 1)), ((j >> 3) & 1) ^ 1);
+    }
+    if (!ok) break;
+    int idx[8], blk[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int e = (j0 + (q >> 1)) * kTileKeys + (q & 1) * 32 + lane;
+      idx[q] = ((q >> 1) < nb && e < p.topk) ? __ldg(tk + e) : -1;
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const bool valid = idx[q] >= 0 && idx[q] < act;
+      const int slot = idx[q] >> 7;
+      blk[q] = (valid && slot < p.mbps) ? __ldg(bt + slot) : -1;
+      if (valid && (blk[q] < 0 || blk[q] >= p.num_blocks)) bad = true;
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if ((q >> 1) >= nb) continue;
+      const bool valid = idx[q] >= 0 && idx[q] < act && blk[q] >= 0 && blk[q] < p.num_blocks;
+      const int j = j0 + (q >> 1);
+      rows[(j & (kIdxSlots - 1)) * kTileKeys + (q & 1) * 32 + lane] = valid ? (blk[q] * 128 + (idx[q] & 127)) : -1;
+    }
+    for (int k = 0; k < nb; ++k) mbar_arrive(c.bar(kBarIdxFull + ((j0 + k) & (kIdxSlots - 1))));
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&g_mla_status, MLA_DEVICE_BAD_BLOCK);
+}
+
+// ------------------------------------------------------------------ gather warps
+// Dequantise 4 int8 values (one word) with one fp32 scale: bf16(fp32(q) * s),
+// as two bf16x2 words ("INT8 quantization path": INT8 -> FP16 -> FP32, times
+// the group scale, -> BF16; the INT8 -> FP32 widening is exact).
+__device__ __forceinline__ void dequant4(uint32_t w, float s, uint32_t& lo, uint32_t& hi) {
+  const float f0 = __fmul_rn(__int2float_rn(static_cast<int>(w << 24) >> 24), s);
+  const float f1 = __fmul_rn(__int2float_rn(static_cast<int>(w << 16) >> 24), s);
+  const float f2 = __fmul_rn(__int2float_rn(static_cast<int>(w << 8) >> 24), s);
+  const float f3 = __fmul_rn(__int2float_rn(static_cast<int>(w) >> 24), s);
+  lo = pack_bf16x2(f0, f1);
+  hi = pack_bf16x2(f2, f3);
+}
+
+// Stage layout (per 64-key tile): chunks 0-3 hold latent dims [64c, 64c+64)
+// of this CTA's half, chunk 4 the rope half in the first 64 bytes of each
+// 128-byte row; row = key, 16-byte unit u of row k stored at unit u ^ (k & 7).
+template <bool kInt8>
+__device__ void gather_role(const Params& p, const Ctx& c, int gw, int lane) {
+  const int g = gw >> 2;   // tile parity handled by this group
+  const int w4 = gw & 3;   // warp within the group: keys [16*w4, 16*w4+16)
+  const int32_t* rows_all = reinterpret_cast<const int32_t*>(c.smem + kOffRows);
+  uint16_t* vmask = reinterpret_cast<uint16_t*>(c.smem + kOffVmask);
+  const uint8_t* kv_rope = reinterpret_cast<const uint8_t*>(p.kv_rope);
+  const int key0 = w4 * 16;
+  const int ru = lane & 3;
+  for (int j = g; j < p.n_tiles; j += 2) {
+    const int st = j & (kStages - 1);
+    const int slot = j & (kIdxSlots - 1);
+    if (!warp_wait(c, kBarEmpty + st, ((j >> 2) & 1) ^ 1)) break;
+    if (!warp_wait(c, kBarIdxFull + slot, (j >> 3) & 1)) break;
+    const int32_t* rows = rows_all + slot * kTileKeys + key0;
+    int32_t myrow[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) myrow[i] = rows[i];
+    const int32_t rope_row0 = rows[lane >> 2];
+    const int32_t rope_row1 = rows[8 + (lane >> 2)];
+    const uint32_t vbits = __ballot_sync(0xffffffffu, lane < 16 && rows[lane & 15] >= 0) & 0xFFFFu;
+    mbar_arrive(c.bar(kBarIdxEmpty + slot));
+    const uint32_t stage = c.sbase + kOffStages + st * kStageBytes;
+    const uint32_t rope_chunk = stage + 4 * kChunkBytes;
+    const int k0 = key0 + (lane >> 2), k1 = key0 + 8 + (lane >> 2);
+    if constexpr (!kInt8) {
+      // latent half: 512 B per key = 32 lanes x 16 B, one row per warp instruction
+      const uint8_t* kvn = reinterpret_cast<const uint8_t*>(p.kv_nope) + c.crank * 512 + lane * 16;
+      const uint32_t chunk = stage + (lane >> 3) * kChunkBytes;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int key = key0 + i;
+        const int32_t row = myrow[i];
+        cp_async_16(chunk + key * 128 + (((lane & 7) ^ (key & 7)) << 4),
+                    row >= 0 ? kvn + static_cast<int64_t>(row) * 1024 : kvn, row >= 0 ? 16u : 0u);
+      }
+      const uint8_t* kvr = kv_rope + c.crank * 64 + ru * 16;
+      cp_async_16(rope_chunk + k0 * 128 + ((ru ^ (k0 & 7)) << 4),
+                  rope_row0 >= 0 ? kvr + static_cast<int64_t>(rope_row0) * 128 : kvr, rope_row0 >= 0 ? 16u : 0u);
+      cp_async_16(rope_chunk + k1 * 128 + ((ru ^ (k1 & 7)) << 4),
+                  rope_row1 >= 0 ? kvr + static_cast<int64_t>(rope_row1) * 128 : kvr, rope_row1 >= 0 ? 16u : 0u);
+      cp_async_arrive_noinc(c.bar(kBarFull + st));
+    } else {
+      const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+      const uint4 r0 = rope_row0 >= 0 ? ldg16(kv_rope + static_cast<int64_t>(rope_row0) * 128 + c.crank * 64 + ru * 16) : zero;
+      const uint4 r1 = rope_row1 >= 0 ? ldg16(kv_rope + static_cast<int64_t>(rope_row1) * 128 + c.crank * 64 + ru * 16) : zero;
+      // latent half: 256 int8 per key = 16 lanes x 16 B; lanes 16-31 take the next key
+      const int u = lane & 15;
+      const int8_t* kvn = reinterpret_cast<const int8_t*>(p.kv_nope) + c.crank * 256 + u * 16;
+      const float* scl = p.kv_scales + c.crank * 2 + (u >> 3);
+      uint4 v[8];
+      float sc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int32_t row = rows[2 * i + (lane >> 4)];
+        v[i] = row >= 0 ? ldg16(kvn + static_cast<int64_t>(row) * 512) : zero;
+        sc[i] = row >= 0 ? __ldg(scl + static_cast<int64_t>(row) * 4) : 0.f;
+      }
+      const uint32_t chunk = stage + (u >> 2) * kChunkBytes;
+      const int u8 = (u & 3) * 2;  // first 8-element unit of these 16 dims within the chunk
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int key = key0 + 2 * i + (lane >> 4);
+        uint4 a, b2;
+        dequant4(v[i].x, sc[i], a.x, a.y);
+        dequant4(v[i].y, sc[i], a.z, a.w);
+        dequant4(v[i].z, sc[i], b2.x, b2.y);
+        dequant4(v[i].w, sc[i], b2.z, b2.w);
+        sts16(chunk + key * 128 + ((u8 ^ (key & 7)) << 4), a);
+        sts16(chunk + key * 128 + (((u8 + 1) ^ (key & 7)) << 4), b2);
+      }
+      sts16(rope_chunk + k0 * 128 + ((ru ^ (k0 & 7)) << 4), r0);
+      sts16(rope_chunk + k1 * 128 + ((ru ^ (k1 & 7)) << 4), r1);
+      fence_proxy_async_smem();
+      mbar_arrive(c.bar(kBarFull + st));
+    }
+    if (lane == 0) {
+      vmask[st * 4 + w4] = static_cast<uint16_t>(vbits);
+      mbar_arrive(c.bar(kBarFull + st));  // releases the mask word
+    }
+  }
+}
+
+// ------------------------------------------------------------------ MMA warp
+__device__ __forceinline__ bool issue_pv(const Ctx& c, int i) {
+  if (!wait_bar(c, kBarPFull, i & 1)) return false;
+  tc_fence_after();
+  constexpr uint32_t idesc = make_idesc_f16(128, 256, 1, 0, 1);
+  const uint32_t stage = c.sbase + kOffStages + (i & (kStages - 1)) * kStageBytes;
+  // O += P_hi . V, then O += P_lo . V (same V tile, K = 16 keys per instruction)
+#pragma unroll
+  for (int s = 0; s < 8; ++s)
+    umma_ts(c.tmem + kTmemO, c.tmem + (s < 4 ? kTmemPhi : kTmemPlo) + 8 * (s & 3),
+            make_sdesc(stage + (s & 3) * 16 * 128, kChunkBytes, 1024, kSwizzle128B), idesc,
+            (i > 0 || s > 0) ? 1u : 0u);
+  umma_commit(c.bar(kBarPvDone));
+  umma_commit(c.bar(kBarEmpty + (i & (kStages - 1))));
+  return true;
+}
+
+__device__ void mma_role(const Params& p, const Ctx& c) {
+  constexpr uint32_t idesc_s = make_idesc_f16(128, 64, 1, 0, 0);
+  const uint32_t qrope = c.sbase + kOffQRope;
+  bool ok = wait_bar(c, kBarQReady, 0);
+  int j = 0;
+  for (; ok && j < p.n_tiles; ++j) {
+    const int st = j & (kStages - 1);
+    if (!wait_bar(c, kBarFull + st, (j >> 2) & 1)) { ok = false; break; }
+    if (j > 0 && !wait_bar(c, kBarSFree, (j - 1) & 1)) { ok = false; break; }
+    fence_proxy_async_smem();  // cp.async data (generic proxy) -> tensor-core reads
+    tc_fence_after();
+    const uint32_t stage = c.sbase + kOffStages + st * kStageBytes;
+#pragma unroll
+    for (int s = 0; s < 16; ++s)
+      umma_ts(c.tmem + kTmemS, c.tmem + kTmemQ + 8 * s,
+              make_sdesc(stage + (s >> 2) * kChunkBytes + (s & 3) * 32, 16, 1024, kSwizzle128B), idesc_s,
+              s > 0 ? 1u : 0u);
+#pragma unroll
+    for (int s = 0; s < 2; ++s)
+      umma_ss(c.tmem + kTmemS, make_sdesc(qrope + s * 32, 16, 1024, kSwizzle128B),
+              make_sdesc(stage + 4 * kChunkBytes + s * 32, 16, 1024, kSwizzle128B), idesc_s, 1u);
+    umma_commit(c.bar(kBarSFull));
+    if (j > 0 && !issue_pv(c, j - 1)) { ok = false; break; }
+  }
+  if (ok) issue_pv(c, p.n_tiles - 1);
+  // Drain: every MMA issued above must finish before TMEM is released.
+  umma_commit(c.bar(kBarFinal));
+  volatile uint32_t never = 0;
+  mbar_wait<false>(c.bar(kBarFinal), 0, &never, kWaitLimitNs);
+}
+
+// ------------------------------------------------------------------ softmax warps
+__device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) {
+  const int h = warp * 32 + lane;
+  const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+  const uint32_t tS = c.tmem + lane_off + kTmemS;
+  const uint32_t tPhi = c.tmem + lane_off + kTmemPhi;
+  const uint32_t tPlo = c.tmem + lane_off + kTmemPlo;
+  const uint32_t tO = c.tmem + lane_off + kTmemO;
+  const uint32_t tQ = c.tmem + lane_off + kTmemQ;
+  const bool live = h < p.n_q;
+  const int64_t qrow = static_cast<int64_t>(c.t) * p.n_q + h;
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  // Q half row: latent part (bf16 pairs) -> TMEM lane h, rope part -> shared
+  // memory row h (the A operand of the two rope MMA steps).
+  {
+    const uint8_t* qn = reinterpret_cast<const uint8_t*>(p.q_nope) + (qrow * 512 + c.crank * 256) * 2;
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch) {
+      uint32_t w[32];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint4 v = live ? ldg16(qn + (ch * 8 + u) * 16) : zero;
+        w[4 * u + 0] = v.x;
+        w[4 * u + 1] = v.y;
+        w[4 * u + 2] = v.z;
+        w[4 * u + 3] = v.w;
+      }
+      tmem_st_32x32b_x32(tQ + 32 * ch, w);
+    }
+    const uint8_t* qr = reinterpret_cast<const uint8_t*>(p.q_rope) + (qrow * 64 + c.crank * 32) * 2;
+    const uint32_t qrope_row = c.sbase + kOffQRope + h * 128;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint4 v = live ? ldg16(qr + u * 16) : zero;
+      sts16(qrope_row + ((u ^ (h & 7)) << 4), v);
+    }
+    fence_proxy_async_smem();
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(c.bar(kBarQReady));
+  }
+  const uint32_t peer = c.crank ^ 1u;
+  const uint32_t recv_local = c.sbase + kOffRecv + h * 256;
+  const uint32_t recv_remote = mapa_shared(recv_local, peer);
+  const uint32_t recv_full_remote = mapa_shared(c.bar(kBarRecvFull), peer);
+  const uint32_t peer_free_remote = mapa_shared(c.bar(kBarPeerFree), peer);
+  const uint32_t sw = static_cast<uint32_t>(h & 15);
+  const uint16_t* vmask = reinterpret_cast<const uint16_t*>(c.smem + kOffVmask);
+  const float scl = p.scale_log2;
+  float m = -INFINITY, l = 0.f;
+  bool ok = true;
+  for (int j = 0; j < p.n_tiles; ++j) {
+    if (!warp_wait(c, kBarSFull, j & 1)) { ok = false; break; }
+    tc_fence_after();
+    uint32_t r[64];
+    tmem_ld_32x32b_x64(tS, r);
+    tmem_wait_ld();
+    tc_fence_before();
+    mbar_arrive(c.bar(kBarSFree));
+    // exchange partial scores with the peer CTA
+    if (j > 0 && !warp_wait_cluster(c, kBarPeerFree, (j - 1) & 1)) { ok = false; break; }
+#pragma unroll
+    for (int u = 0; u < 16; ++u)
+      st_async_v4(recv_remote + ((u ^ sw) << 4), r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3], recv_full_remote);
+    if (!warp_wait_cluster(c, kBarRecvFull, j & 1)) { ok = false; break; }
+    if (h == 0 && j + 1 < p.n_tiles) mbar_arrive_expect_tx(c.bar(kBarRecvFull), kRecvBytes);
+    float s[64];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const float4 v = lds16f(recv_local + ((u ^ sw) << 4));
+      s[4 * u + 0] = __uint_as_float(r[4 * u + 0]) + v.x;
+      s[4 * u + 1] = __uint_as_float(r[4 * u + 1]) + v.y;
+      s[4 * u + 2] = __uint_as_float(r[4 * u + 2]) + v.z;
+      s[4 * u + 3] = __uint_as_float(r[4 * u + 3]) + v.w;
+    }
+    mbar_arrive_remote(peer_free_remote);
+    // validity of the tile's 64 entries (acquire the gather's writes)
+    if (!warp_wait(c, kBarFull + (j & (kStages - 1)), (j >> 2) & 1)) { ok = false; break; }
+    const uint16_t* vm16 = vmask + (j & (kStages - 1)) * 4;
+    const uint64_t vm = static_cast<uint64_t>(vm16[0]) | (static_cast<uint64_t>(vm16[1]) << 16) |
+                        (static_cast<uint64_t>(vm16[2]) << 32) | (static_cast<uint64_t>(vm16[3]) << 48);
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      s[i] = ((vm >> i) & 1ull) ? s[i] * scl : -INFINITY;
+      mx = fmaxf(mx, s[i]);
+    }
+    // Lazy rescale: the running max m only moves when a head's tile max exceeds
+    // it by more than 8 (log2 units), so P stays <= 2^8 and O is rescaled rarely.
+    const bool grow = mx > m + 8.f;
+    const float f = grow ? fast_exp2(m - mx) : 1.f;  // m = -inf -> 0
+    if (grow) {
+      l *= f;
+      m = mx;
+    }
+    if (__any_sync(0xffffffffu, grow) && j > 0) {
+      // TMEM accesses are warp-collective: the whole warp waits for the previous
+      // P.V, then every lane rescales its own O row (f = 1 where m did not move).
+      if (!warp_wait(c, kBarPvDone, (j - 1) & 1)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll 1
+      for (int ch = 0; ch < 16; ++ch) {
+        uint32_t o[16];
+        tmem_ld_32x32b_x16(tO + 16 * ch, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+        tmem_st_32x32b_x16(tO + 16 * ch, o);
+      }
+      tmem_wait_st();
+    }
+    const float mm = (m == -INFINITY) ? 0.f : m;
+    uint32_t phi[32], plo[32];
+    float lsum = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float p0 = fast_exp2(s[2 * i] - mm);
+      const float p1 = fast_exp2(s[2 * i + 1] - mm);
+      lsum += p0 + p1;
+      const uint32_t hw = pack_bf16x2(p0, p1);
+      phi[i] = hw;
+      // p - bf16(p) is exact in fp32; its bf16 rounding leaves an error <= 2^-18 p
+      plo[i] = pack_bf16x2(p0 - __uint_as_float(hw << 16), p1 - __uint_as_float(hw & 0xFFFF0000u));
+    }
+    l += lsum;
+    if (j > 0) {
+      if (!warp_wait(c, kBarPvDone, (j - 1) & 1)) { ok = false; break; }
+      tc_fence_after();
+    }
+    tmem_st_32x32b_x32(tPhi, phi);
+    tmem_st_32x32b_x32(tPlo, plo);
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(c.bar(kBarPFull));
+  }
+  if (!ok) return;
+  if (!warp_wait(c, kBarPvDone, (p.n_tiles - 1) & 1)) return;
+  tc_fence_after();
+  const float inv_l = l > 0.f ? 1.f / l : 0.f;
+  uint4* op = reinterpret_cast<uint4*>(p.out + qrow * 512 + c.crank * 256);
+#pragma unroll 1
+  for (int ch = 0; ch < 8; ++ch) {
+    uint32_t o[32];
+    tmem_ld_32x32b_x32(tO + 32 * ch, o);
+    tmem_wait_ld();
+    if (live) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint4 w;
+        w.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l);
+        w.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l);
+        w.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l);
+        w.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l);
+        op[ch * 4 + k] = w;
+      }
+    }
+  }
+  if (live && c.crank == 0 && p.lse != nullptr)
+    p.lse[qrow] = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+}
+
+// ------------------------------------------------------------------ kernel
+template <bool kInt8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_sparse_fwd_kernel(const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  Ctx c;
+  c.smem = smem;
+  c.sbase = smem_u32(smem);
+  c.crank = cluster_ctarank();
+  c.t = blockIdx.x >> 1;
+  c.abort = reinterpret_cast<volatile uint32_t*>(smem + kOffAbort);
+  if (tid == 0) {
+    *c.abort = (*reinterpret_cast<volatile unsigned int*>(&g_mla_status) & MLA_DEVICE_TIMEOUT) ? 1u : 0u;
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(c.bar(kBarFull + i), 128 + 4);
+      mbar_init(c.bar(kBarEmpty + i), 1);
+    }
+    for (int i = 0; i < kIdxSlots; ++i) {
+      mbar_init(c.bar(kBarIdxFull + i), 32);
+      mbar_init(c.bar(kBarIdxEmpty + i), 128);
+    }
+    mbar_init(c.bar(kBarSFull), 1);
+    mbar_init(c.bar(kBarSFree), 128);
+    mbar_init(c.bar(kBarPFull), 128);
+    mbar_init(c.bar(kBarPvDone), 1);
+    mbar_init(c.bar(kBarRecvFull), 1);
+    mbar_init(c.bar(kBarPeerFree), 128);
+    mbar_init(c.bar(kBarQReady), 128);
+    mbar_init(c.bar(kBarFinal), 1);
+    fence_mbarrier_init_cluster();
+    mbar_arrive_expect_tx(c.bar(kBarRecvFull), kRecvBytes);  // phase 0 of the score exchange
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(c.sbase + kOffTmemSlot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  cluster_arrive();
+  cluster_wait();
+  tc_fence_after();
+  c.tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmemSlot);
+
+  if (!*c.abort) {
+    if (warp < kGatherWarp0) {
+      softmax_role(p, c, warp, lane);
+    } else if (warp < kMmaWarp) {
+      gather_role<kInt8>(p, c, warp - kGatherWarp0, lane);
+    } else if (warp == kMmaWarp) {
+      if (lane == 0) mma_role(p, c);
+      __syncwarp();
+    } else {
+      index_role(p, c, lane);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(c.tmem, kTmemCols);
+  if (tid == 0 && *c.abort) atomicOr(&g_mla_status, MLA_DEVICE_TIMEOUT);
+  // Neither CTA may exit while its peer could still address its shared memory.
+  cluster_arrive();
+  cluster_wait();
+}
+
+}  // namespace mlasp
+
+// ==================================================================== C ABI
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+mla_status fail(mla_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+mla_status fail(mla_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0; }
+
+constexpr int kMaxDevices = 64;
+std::once_flag g_attr_once[kMaxDevices][2];
+cudaError_t g_attr_err[kMaxDevices][2];
+
+template <bool kInt8>
+cudaError_t prepare_kernel(int dev) {
+  std::call_once(g_attr_once[dev][kInt8 ? 1 : 0], [dev] {
+    g_attr_err[dev][kInt8 ? 1 : 0] = cudaFuncSetAttribute(
+        mlasp::mla_sparse_fwd_kernel<kInt8>, cudaFuncAttributeMaxDynamicSharedMemorySize, mlasp::kSmemBytes);
+  });
+  return g_attr_err[dev][kInt8 ? 1 : 0];
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t mla_sparse_abi_version(void) { return 100; }
+
+const char* mla_sparse_last_error(void) { return g_last_error; }
+
+mla_status mla_sparse_attn_fwd(const mla_dims* dims, const void* q_nope, const void* q_rope, const void* kv_nope,
+                               const void* kv_rope, const float* kv_scales, const int32_t* topk_idx,
+                               const int32_t* block_table, const int32_t* act_seqs, void* out, float* lse,
+                               float softmax_scale, int32_t mode, void* stream) {
+  g_last_error[0] = '\0';
+  if (dims == nullptr) return fail(MLA_ERR_NULL, "dims is NULL");
+  const mla_dims d = *dims;
+  if (!q_nope || !q_rope || !kv_nope || !kv_rope || !topk_idx || !block_table || !act_seqs || !out)
+    return fail(MLA_ERR_NULL, "a required tensor pointer is NULL");
+  if (d.kv_dtype != MLA_KV_BF16 && d.kv_dtype != MLA_KV_INT8)
+    return fail(MLA_ERR_DTYPE, "kv_dtype %d is neither MLA_KV_BF16 nor MLA_KV_INT8", d.kv_dtype);
+  if (d.kv_dtype == MLA_KV_INT8 && kv_scales == nullptr)
+    return fail(MLA_ERR_DTYPE, "kv_scales is required for an INT8 cache");
+  if (d.B < 1 || d.S1 < 1 || d.topk < 1 || d.num_blocks < 1 || d.max_blocks_per_seq < 1)
+    return fail(MLA_ERR_SHAPE, "B, S1, topk, num_blocks and max_blocks_per_seq must be >= 1");
+  if (d.n_q < 1 || d.n_q > 128) return fail(MLA_ERR_SHAPE, "n_q=%d outside [1, 128]", d.n_q);
+  if (d.n_kv != 1) return fail(MLA_ERR_UNSUPPORTED, "n_kv=%d: only one latent KV head is implemented", d.n_kv);
+  if (d.d_nope != 512 || d.d_rope != 64 || d.block_size != 128)
+    return fail(MLA_ERR_UNSUPPORTED, "d_nope=%d d_rope=%d block_size=%d: only 512/64/128 are implemented", d.d_nope,
+                d.d_rope, d.block_size);
+  if (d.num_blocks >= (1 << 24)) return fail(MLA_ERR_SHAPE, "num_blocks=%d must be < 2^24", d.num_blocks);
+  const int64_t T = static_cast<int64_t>(d.B) * d.S1;
+  if (T > (1ll << 30)) return fail(MLA_ERR_SHAPE, "B*S1=%lld too large", static_cast<long long>(T));
+  if (mode != MLA_MODE_DECODE && mode != MLA_MODE_PREFILL) return fail(MLA_ERR_SHAPE, "mode %d unknown", mode);
+  if (!isfinite(softmax_scale)) return fail(MLA_ERR_SHAPE, "softmax_scale is not finite");
+  if (!aligned(q_nope, 16) || !aligned(q_rope, 16) || !aligned(kv_nope, 16) || !aligned(kv_rope, 16) ||
+      !aligned(out, 16) || (kv_scales && d.kv_dtype == MLA_KV_INT8 && !aligned(kv_scales, 16)))
+    return fail(MLA_ERR_ALIGN, "q/kv/out/scales pointers must be 16-byte aligned");
+  if (!aligned(topk_idx, 4) || !aligned(block_table, 4) || !aligned(act_seqs, 4) || (lse && !aligned(lse, 4)))
+    return fail(MLA_ERR_ALIGN, "index tensors and lse must be 4-byte aligned");
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(MLA_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
+  const bool int8 = d.kv_dtype == MLA_KV_INT8;
+  e = int8 ? prepare_kernel<true>(dev) : prepare_kernel<false>(dev);
+  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+
+  mlasp::Params p;
+  p.q_nope = static_cast<const uint16_t*>(q_nope);
+  p.q_rope = static_cast<const uint16_t*>(q_rope);
+  p.kv_nope = kv_nope;
+  p.kv_rope = static_cast<const uint16_t*>(kv_rope);
+  p.kv_scales = int8 ? kv_scales : nullptr;
+  p.topk_idx = topk_idx;
+  p.block_table = block_table;
+  p.act_seqs = act_seqs;
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
+  p.S1 = d.S1;
+  p.n_q = d.n_q;
+  p.topk = d.topk;
+  p.num_blocks = d.num_blocks;
+  p.mbps = d.max_blocks_per_seq;
+  p.n_tiles = (d.topk + mlasp::kTileKeys - 1) / mlasp::kTileKeys;
+  p.scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634);
+  const dim3 grid(static_cast<unsigned>(2 * T));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (int8)
+    mlasp::mla_sparse_fwd_kernel<true><<<grid, mlasp::kThreads, mlasp::kSmemBytes, s>>>(p);
+  else
+    mlasp::mla_sparse_fwd_kernel<false><<<grid, mlasp::kThreads, mlasp::kSmemBytes, s>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
+  return MLA_OK;
+}
+
+mla_status mla_sparse_device_status(void* stream, uint32_t* flags, int32_t clear) {
+  g_last_error[0] = '\0';
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
+  unsigned int v = 0;
+  e = cudaMemcpyFromSymbol(&v, mlasp::g_mla_status, sizeof v);
+  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "reading the status word: %s", cudaGetErrorString(e));
+  if (clear) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(mlasp::g_mla_status, &zero, sizeof zero);
+    if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "clearing the status word: %s", cudaGetErrorString(e));
+  }
+  if (flags) *flags = v;
+  if (v != 0) return fail(MLA_ERR_DEVICE_STATUS, "device status 0x%x", v);
+  return MLA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,115 @@
+"""Host-side checks of the C ABI: the library builds, loads, exports every
+function include/mla_sparse.h declares, and rejects bad arguments before
+touching the GPU (every case below fails validation, so no CUDA call runs)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mla_sparse.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mla_sparse_top_gb300 import build, binding
+    build.build()
+    return binding.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_sparse_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    assert {"mla_sparse_attn_fwd", "mla_sparse_last_error", "mla_sparse_device_status",
+            "mla_sparse_abi_version"} <= set(names)
+
+
+def test_library_exports_every_declared_function(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    from mla_sparse_top_gb300 import binding
+    assert set(binding.EXPORTED_SYMBOLS) == set(declared_functions())
+    assert lib.mla_sparse_abi_version() == 100
+
+
+def _dims(**kw):
+    from mla_sparse_top_gb300.binding import MlaDims
+    d = dict(B=2, S1=2, n_q=128, n_kv=1, d_nope=512, d_rope=64, block_size=128, num_blocks=16,
+             max_blocks_per_seq=8, topk=2048, kv_dtype=0)
+    d.update(kw)
+    return MlaDims(**d)
+
+
+def _call(lib, dims, ptrs=None, scales=None, scale=0.04, mode=0):
+    p = ptrs if ptrs is not None else [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(9)]
+    q_nope, q_rope, kv_nope, kv_rope, topk, bt, act, out, lse = p
+    return lib.mla_sparse_attn_fwd(None if dims is None else ctypes.byref(dims), q_nope, q_rope, kv_nope,
+                                   kv_rope, scales, topk, bt, act, out, lse, ctypes.c_float(scale),
+                                   ctypes.c_int32(mode), None)
+
+
+@pytest.mark.parametrize("case,expect", [
+    ("null_dims", -1), ("null_q", -1), ("bad_dtype", -3), ("int8_no_scales", -3), ("n_q_zero", -2),
+    ("n_q_big", -2), ("n_kv_2", -4), ("d_nope_256", -4), ("block_64", -4), ("topk_zero", -2),
+    ("mode_bad", -2), ("scale_nan", -2), ("misaligned_kv", -5), ("misaligned_topk", -5), ("batch_zero", -2),
+    ("blocks_huge", -2),
+])
+def test_argument_errors_are_reported_before_launch(lib, case, expect):
+    dims = _dims()
+    ptrs = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(9)]
+    scales = None
+    scale = 0.04
+    mode = 0
+    if case == "null_dims":
+        dims = None
+    elif case == "null_q":
+        ptrs[0] = None
+    elif case == "bad_dtype":
+        dims = _dims(kv_dtype=7)
+    elif case == "int8_no_scales":
+        dims = _dims(kv_dtype=1)
+    elif case == "n_q_zero":
+        dims = _dims(n_q=0)
+    elif case == "n_q_big":
+        dims = _dims(n_q=129)
+    elif case == "n_kv_2":
+        dims = _dims(n_kv=2)
+    elif case == "d_nope_256":
+        dims = _dims(d_nope=256)
+    elif case == "block_64":
+        dims = _dims(block_size=64)
+    elif case == "topk_zero":
+        dims = _dims(topk=0)
+    elif case == "mode_bad":
+        mode = 5
+    elif case == "scale_nan":
+        scale = float("nan")
+    elif case == "misaligned_kv":
+        ptrs[2] = ctypes.c_void_p(0x20008)
+    elif case == "misaligned_topk":
+        ptrs[4] = ctypes.c_void_p(0x50002)
+    elif case == "batch_zero":
+        dims = _dims(B=0)
+    elif case == "blocks_huge":
+        dims = _dims(num_blocks=1 << 24)
+    st = _call(lib, dims, ptrs, scales, scale, mode)
+    assert st == expect
+    assert lib.mla_sparse_last_error().decode() != ""
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    from mla_sparse_top_gb300 import binding
+    with pytest.raises(RuntimeError):
+        binding.ctypes  # noqa: B018  (module is importable)
+        saved = binding._lib
+        binding._lib = None
+        try:
+            binding.load_library(str(tmp_path / "missing.so"))
+        finally:
+            binding._lib = saved

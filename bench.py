@@ -1,0 +1,395 @@
+"""Benchmark: sparse MLA attention over a paged KV cache on GB300.
+
+Default workload: MTP decode, B=64 S1=2 N_Q=128 topk=2048, act_seq 8192 for
+every batch entry, 4096 shuffled 128-row blocks, bf16 cache (seeded synthetic
+N(0,1) data).  One step = one call of the fused kernel over the whole batch.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  ``value`` is microseconds per call (the
+device-timed kernel, CUDA events on the launching stream, L2 flushed by a
+256 MiB write between timed calls); ``e2e`` is the same call made through the
+C ABI with the step's inputs copied from pinned host memory and the outputs
+copied back inside the timed region.  Under torchrun every rank runs its own
+batch (weak scaling, no collective on the data path); the reported time is
+the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "sparse MLA attn µs/call, gathered-KV TB/s & % roofline (B64 S1=2 topk2048)"
+UNIT = "us/call"
+KERNEL_NAME = "mla_sparse_fwd_kernel"
+KERNEL_SOURCE = os.path.join(ROOT, "mla_sparse_top_gb300", "csrc", "mla_sparse_fwd.cu")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mtp_decode", choices=sorted(workloads.NAMED))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ accounting
+def row_bytes(inp):
+    return (512 + 4 * 4 + 128) if inp["dims"]["kv_int8"] else (1024 + 128)
+
+
+def valid_mask(inp):
+    d = inp["dims"]
+    act = np.repeat(inp["act_seqs"], d["S1"])[:, None]
+    tk = inp["topk_idx"]
+    return (tk >= 0) & (tk < act)
+
+
+def algorithmic_counts(inp):
+    """Method's own work: SURVEY-style counts from the actual inputs."""
+    d = inp["dims"]
+    T, H = d["B"] * d["S1"], d["n_q"]
+    vm = valid_mask(inp)
+    n_valid = int(vm.sum())
+    rb = row_bytes(inp)
+    # unique physical rows touched, per batch entry (tokens of one batch entry share rows)
+    uniq = 0
+    for b in range(d["B"]):
+        sel = inp["topk_idx"][b * d["S1"]:(b + 1) * d["S1"]][vm[b * d["S1"]:(b + 1) * d["S1"]]]
+        uniq += int(np.unique(sel).size)
+    io = T * H * (512 + 64) * 2 + T * H * 512 * 2 + T * H * 4 + T * d["topk"] * 4 + inp["block_table"].nbytes \
+        + inp["act_seqs"].nbytes
+    return dict(n_valid=n_valid, gathered_bytes=n_valid * rb, roofline_bytes=uniq * rb + io,
+                flops=2.0 * H * n_valid * (576 + 512))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for fn in (KERNEL_SOURCE, os.path.join(ROOT, "mla_sparse_top_gb300", "csrc", "ptx.cuh")):
+        with open(fn, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (otherwise None)."""
+    fn = os.path.join(ROOT, "profiles", f"{KERNEL_NAME}_{workload}.md")
+    if not os.path.exists(fn):
+        return None
+    text = open(fn).read()
+    mh = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    mt = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not mh or not mt or mh.group(1) != kernel_source_hash():
+        return None
+    return float(mt.group(1))
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.t_on = self.t_off = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark_on(self):
+        self.t_on = time.time()
+
+    def mark_off(self):
+        self.t_off = time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return self.summary()
+
+    def summary(self):
+        rows = []
+        for ts, line in self.samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((ts, parts))
+        inside = [r for r in rows if self.t_on is not None and self.t_on - 0.05 <= r[0] <= (self.t_off or 1e30) + 0.05]
+        use = inside if inside else rows[-3:]
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        mhz = [float(p[1]) for _, p in use if p[1].replace(".", "").isdigit()]
+        mx = [float(p[2]) for _, p in use if p[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, p in use:
+            for k, name in enumerate(names):
+                if p[5 + k].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(mhz)) if mhz else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(use), "in_timed_region": bool(inside)}
+
+
+# ------------------------------------------------------------------ CPU oracle sample
+def time_oracle(inp, target_s: float):
+    """Time the oracle, as it stands, on a bounded token sample; returns
+    (us per full call, cores, sample description)."""
+    import oracle
+    oracle.build()
+    T = inp["dims"]["B"] * inp["dims"]["S1"]
+    cores = oracle.max_threads()
+    t0 = time.perf_counter()
+    oracle.forward(inp, tokens=[0])
+    t1 = time.perf_counter() - t0
+    n = int(max(1, min(T, round(target_s / max(t1, 1e-6)))))
+    n = max(n, min(T, cores))
+    toks = list(range(n))
+    t0 = time.perf_counter()
+    oracle.forward(inp, tokens=toks)
+    dt = time.perf_counter() - t0
+    us = dt / n * T * 1e6
+    return us, cores, f"first {n} of {T} tokens in one oracle call ({dt:.2f} s), scaled to all {T} tokens"
+
+
+# ------------------------------------------------------------------ main
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    import torch
+    import torch.distributed as dist
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    import mla_sparse_top_gb300 as mla
+    from mla_sparse_top_gb300 import build
+    build.build()
+    mla.load_library()
+
+    # every rank draws its own batch (weak scaling)
+    gen = workloads.NAMED[args.workload]
+    inp = gen(seed={"tiny_decode": 0, "mtp_decode": 1, "int8_decode": 2, "varlen_decode": 3,
+                    "prefill": 4}[args.workload] + 1000 * rank)
+    counts = algorithmic_counts(inp)
+    dev = workloads.to_device(inp)
+    dims = mla.dims_from_workload(inp["dims"])
+    stream = torch.cuda.current_stream()
+    mode = inp.get("mode", "decode")
+
+    def launch():
+        mla.mla_sparse_attn_fwd(dev["q_nope"], dev["q_rope"], dev["kv_nope"], dev["kv_rope"], dev["kv_scales"],
+                                dev["topk_idx"], dev["block_table"], dev["act_seqs"], dev["out"], dev["lse"],
+                                softmax_scale=inp["softmax_scale"], mode=mode, dims=dims, stream=stream)
+
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    for i in range(max(3, args.warmup)):
+        flush.fill_(float(i))
+        launch()
+    torch.cuda.synchronize()
+    if mla.device_status(clear=True):
+        raise RuntimeError("device status reported an error during warm-up")
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.15)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.mark_on()
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        starts[i].record(stream)
+        launch()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    clocks.mark_off()
+    if world > 1:
+        dist.barrier()
+    times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    status = mla.device_status(clear=True)
+
+    # end-to-end through the C ABI with host buffers (pinned), copies inside the timed region
+    host_in = {k: dev[k].cpu().pin_memory() for k in ("q_nope", "q_rope", "topk_idx", "block_table", "act_seqs")}
+    host_out = dev["out"].cpu().pin_memory()
+    host_lse = dev["lse"].cpu().pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * host_lse.element_size()
+    e2e_steps = max(5, min(args.steps, 50))
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    for i in range(e2e_steps + 2):
+        flush.fill_(float(i))
+        k = i - 2
+        if k >= 0:
+            e_s[k].record(stream)
+        for name, t in host_in.items():
+            dev[name].copy_(t, non_blocking=True)
+        launch()
+        host_out.copy_(dev["out"], non_blocking=True)
+        host_lse.copy_(dev["lse"], non_blocking=True)
+        if k >= 0:
+            e_e[k].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = [s.elapsed_time(e) for s, e in zip(e_s, e_e)]
+    clock_summary = clocks.stop()
+
+    us = float(np.mean(times_ms) * 1000.0)
+    e2e_us = float(np.mean(e2e_ms) * 1000.0)
+    if world > 1:
+        t = torch.tensor([us, e2e_us], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        us, e2e_us = float(t[0]), float(t[1])
+
+    if rank == 0:
+        hbm_gbs, bf16_tf, peak_src = measured_peaks()
+        achieved_gbs = counts["roofline_bytes"] / (us * 1e-6) / 1e9
+        tflops = counts["flops"] / (us * 1e-6) / 1e12
+        roofline_us = max(counts["roofline_bytes"] / (hbm_gbs * 1e9), counts["flops"] / (bf16_tf * 1e12)) * 1e6
+        traffic = ncu_traffic(args.workload)
+        d = inp["dims"]
+        line = {
+            "metric": METRIC,
+            "value": round(us, 3),
+            "unit": UNIT,
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(us / 1000.0, 6),
+            "higher_is_better": False,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic",
+            "config": {
+                "workload": f"{args.workload}: B={d['B']} S1={d['S1']} N_Q={d['n_q']} topk={d['topk']} "
+                            f"{'int8' if d['kv_int8'] else 'bf16'} paged cache ({d['num_blocks']} blocks of 128)",
+                "B": d["B"], "S1": d["S1"], "n_q": d["n_q"], "topk": d["topk"],
+                "kv_dtype": "int8" if d["kv_int8"] else "bf16",
+                "l2": "flushed between timed calls by a 256 MiB write (outside the per-call events)",
+                "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            },
+            "gathered_kv_tbps": round(counts["gathered_bytes"] * world / (us * 1e-6) / 1e12, 4),
+            "tflops": round(tflops * world, 2),
+            "roofline_us": round(roofline_us, 3),
+            "roofline_frac_of_call": round(roofline_us / us, 4),
+            "roofline": {
+                "bound": "hbm",
+                "achieved": round(achieved_gbs, 1),
+                "peak": hbm_gbs,
+                "unit": "GB/s",
+                "frac": round(achieved_gbs / hbm_gbs, 4),
+                "traffic": traffic,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback",
+                "algorithmic_bytes_per_launch": counts["roofline_bytes"],
+                "kernel": KERNEL_NAME,
+            },
+            "tensor": {"achieved_tflops": round(tflops, 2), "peak_tflops": bf16_tf,
+                       "frac": round(tflops / bf16_tf, 4), "flops_per_launch": counts["flops"]},
+            "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": int(d2h)},
+            "gpu_launches": args.steps,
+            "clocks": clock_summary,
+            "device_status": status,
+        }
+        if not args.no_cpu_baseline:
+            cus, cores, sample = time_oracle(inp, args.cpu_seconds)
+            line["cpu_baseline"] = {"value": round(cus, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+                                    "sample": sample}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the fp64 oracle, as it stands, on the host cores."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    gen = workloads.NAMED[args.workload]
+    inp = gen()
+    d = inp["dims"]
+    T = d["B"] * d["S1"]
+    cores = oracle.max_threads()
+    toks_per_step = max(1, cores)
+    if args.warmup > 0:
+        oracle.forward(inp, tokens=[0])
+    per_call = []
+    for i in range(args.steps):
+        toks = [(i * toks_per_step + k) % T for k in range(toks_per_step)]
+        t0 = time.perf_counter()
+        oracle.forward(inp, tokens=toks)
+        per_call.append((time.perf_counter() - t0) / len(toks) * T * 1e6)
+    us = float(np.mean(per_call))
+    sample = f"{toks_per_step} of {T} tokens per step, scaled to all {T} tokens"
+    line = {
+        "metric": METRIC, "value": round(us, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(us / 1000.0, 3), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": f"{args.workload}: B={d['B']} S1={d['S1']} N_Q={d['n_q']} topk={d['topk']}",
+                   "B": d["B"], "S1": d["S1"], "n_q": d["n_q"], "topk": d["topk"]},
+        "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -5,9 +5,9 @@ The computation lives in ``libmla_sparse.so`` (CUDA for sm_103a, C ABI in
 through a thin ctypes binding with the same entry-point names.
 """
 from .binding import (MLA_DEVICE_BAD_BLOCK, MLA_DEVICE_TIMEOUT, MLA_KV_BF16, MLA_KV_INT8, MLA_MODE_DECODE,
-                      MLA_MODE_PREFILL, MlaDims, MlaError, abi_version, device_status, load_library,
+                      MLA_MODE_PREFILL, MlaDims, MlaError, abi_version, device_status, dims_from_workload, load_library,
                       mla_sparse_attn_fwd)
 
-__all__ = ["mla_sparse_attn_fwd", "device_status", "abi_version", "load_library", "MlaDims", "MlaError",
+__all__ = ["mla_sparse_attn_fwd", "device_status", "abi_version", "load_library", "MlaDims", "MlaError", "dims_from_workload",
            "MLA_MODE_DECODE", "MLA_MODE_PREFILL", "MLA_KV_BF16", "MLA_KV_INT8", "MLA_DEVICE_BAD_BLOCK",
            "MLA_DEVICE_TIMEOUT"]

@@ -79,6 +79,13 @@ def _stream_handle(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def dims_from_workload(d: dict) -> MlaDims:
+    """MlaDims from a dimension dict with the header's field names (kv_int8 flag)."""
+    return MlaDims(B=d["B"], S1=d["S1"], n_q=d["n_q"], n_kv=d["n_kv"], d_nope=d["d_nope"], d_rope=d["d_rope"],
+                   block_size=d["block_size"], num_blocks=d["num_blocks"], max_blocks_per_seq=d["max_blocks_per_seq"],
+                   topk=d["topk"], kv_dtype=MLA_KV_INT8 if d["kv_int8"] else MLA_KV_BF16)
+
+
 def make_dims(q_nope, kv_nope, topk_idx, block_table, kv_int8: bool, S1: int) -> MlaDims:
     T, n_q, d_nope = q_nope.shape
     if T % S1:

@@ -6,6 +6,7 @@ import numpy as np
 import torch
 
 import mla_sparse_top_gb300 as mla
+import workloads
 
 # tolerance: rtol 0.005 / atol 0.0001 on the bf16 output (the operator spec's
 # precision standard), 1e-3 relative on the fp32 lse
@@ -18,30 +19,11 @@ def bf16_to_f64(bits):
 
 
 def to_device(inp: dict, device="cuda") -> dict:
-    d = inp["dims"]
-    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)  # noqa: E731
-    dev = dict(
-        q_nope=bf(inp["q_nope"]),
-        q_rope=bf(inp["q_rope"]),
-        kv_nope=(torch.from_numpy(np.ascontiguousarray(inp["kv_nope"])).to(device) if d["kv_int8"] else bf(inp["kv_nope"])),
-        kv_rope=bf(inp["kv_rope"]),
-        kv_scales=(torch.from_numpy(np.ascontiguousarray(inp["kv_scales"])).to(device) if d["kv_int8"] else None),
-        topk_idx=torch.from_numpy(np.ascontiguousarray(inp["topk_idx"])).to(device),
-        block_table=torch.from_numpy(np.ascontiguousarray(inp["block_table"])).to(device),
-        act_seqs=torch.from_numpy(np.ascontiguousarray(inp["act_seqs"])).to(device),
-    )
-    T, H = d["B"] * d["S1"], d["n_q"]
-    dev["out"] = torch.empty((T, H, d["d_nope"]), dtype=torch.bfloat16, device=device)
-    dev["lse"] = torch.empty((T, H), dtype=torch.float32, device=device)
-    return dev
+    return workloads.to_device(inp, device)
 
 
 def dims_of(inp: dict) -> "mla.MlaDims":
-    d = inp["dims"]
-    return mla.MlaDims(B=d["B"], S1=d["S1"], n_q=d["n_q"], n_kv=d["n_kv"], d_nope=d["d_nope"], d_rope=d["d_rope"],
-                       block_size=d["block_size"], num_blocks=d["num_blocks"],
-                       max_blocks_per_seq=d["max_blocks_per_seq"], topk=d["topk"],
-                       kv_dtype=mla.MLA_KV_INT8 if d["kv_int8"] else mla.MLA_KV_BF16)
+    return mla.dims_from_workload(inp["dims"])
 
 
 def launch(inp: dict, dev: dict, mode=None):

@@ -180,3 +180,23 @@ NAMED = {
     "varlen_decode": varlen_decode,
     "prefill": prefill,
 }
+
+
+def to_device(inp: dict, device="cuda") -> dict:
+    """Copy a workload to the device as torch tensors, plus empty out / lse."""
+    d = inp["dims"]
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+    def raw(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+    dev = dict(q_nope=bf(inp["q_nope"]), q_rope=bf(inp["q_rope"]),
+               kv_nope=raw(inp["kv_nope"]) if d["kv_int8"] else bf(inp["kv_nope"]), kv_rope=bf(inp["kv_rope"]),
+               kv_scales=raw(inp["kv_scales"]) if d["kv_int8"] else None, topk_idx=raw(inp["topk_idx"]),
+               block_table=raw(inp["block_table"]), act_seqs=raw(inp["act_seqs"]))
+    T, H = d["B"] * d["S1"], d["n_q"]
+    dev["out"] = torch.empty((T, H, d["d_nope"]), dtype=torch.bfloat16, device=device)
+    dev["lse"] = torch.empty((T, H), dtype=torch.float32, device=device)
+    return dev

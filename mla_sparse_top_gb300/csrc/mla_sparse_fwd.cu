@@ -2,44 +2,49 @@
 //
 // One query token is processed by a cluster of two CTAs.  CTA r (its rank in
 // the cluster) owns the latent dims [256r, 256r+256) and the rope dims
-// [32r, 32r+32): it gathers only that half of every selected cache row, so no
-// byte is read twice, and it accumulates O[:, its 256 dims] for all 128 heads
-// in tensor memory.  Scores need all 576 dims, so each CTA computes a partial
-// score tile over its half and the two partials are exchanged through
-// distributed shared memory (st.async + mbarrier transaction counts); both
-// CTAs then hold the same full score tile and run the same online softmax.
+// [32r, 32r+32): it gathers only that half of every selected cache row, so
+// every byte is read once, and it accumulates O[:, its 256 latent dims] for
+// all 128 heads in tensor memory (O for a whole token is 128 x 512 fp32 =
+// 256 KB, the entire TMEM of one SM, which is why a token needs two SMs).
+// Scores need all 576 dims: each CTA computes a partial score tile over its
+// 288 dims and sends it (fp32) to the peer through distributed shared memory;
+// both CTAs then hold bit-identical score tiles (fp32 addition commutes) and
+// run the same online softmax.  Sending is done by dedicated warps so that
+// the softmax warps never wait for remote stores to drain, and the softmax
+// runs one tile behind the score MMA so the exchange overlaps with it.
 //
-// Per CTA (448 threads):
-//   warps 0-3   softmax: TMEM lane h = head h.  Load Q (latent part into TMEM,
-//               rope part into shared memory), per key tile read S, exchange
-//               with the peer, mask/scale/online softmax, write P into TMEM as
-//               two bf16 terms P_hi = bf16(p), P_lo = bf16(p - P_hi), rescale
-//               O when the running max grows by more than 2^8, final O / l ->
-//               bf16 and lse.
-//   warps 4-11  gather: two groups of four warps, alternating key tiles; for
-//               each selected row copy the half row into the 128-byte-swizzled
-//               layout of the stage ring (bf16: cp.async with zero fill for
-//               masked entries; int8: load, dequantise to bf16, store).
-//   warp 12     MMA issue (one thread): S = Q.K^T (A = Q in TMEM / smem, B = K
-//               tile, K-major) and O += P_hi.V + P_lo.V (A = P in TMEM, B = V
-//               tile, MN-major), tcgen05 bf16 with FP32 accumulators in TMEM.
+// Per CTA (24 warps; registers rebalanced per warpgroup with setmaxnreg):
+//   warps 0-7   softmax: TMEM lane h = head h; warps w and w+4 share the
+//               lanes of quadrant w % 4 and take key columns [32c, 32c+32),
+//               c = w / 4.  Load Q (latent half into TMEM, rope half into
+//               smem); per tile keep the own partial S, add the peer's, mask
+//               and scale, row max across the warp pair, lazy online softmax,
+//               write P into TMEM as P_hi = bf16(p), P_lo = bf16(p - P_hi);
+//               final O / l -> bf16 and lse.
+//   warps 8-11  senders: read the partial S tile and push it to the peer.
+//   warps 12-19 gather: two groups of four warps, alternating key tiles; bf16
+//               cache by cp.async with zero fill for masked entries, INT8
+//               cache by loads, dequantisation to bf16 and stores.
+//   warp 20     MMA issue (one thread): S = Q K^T (A = Q latent in TMEM, rope
+//               in smem), O += P_hi V + P_lo V (A = P in TMEM, B = V MN-major).
+//   warp 21     index resolution: topk entry -> validity -> block_table -> row.
 //
-// Precision: every product is exact (bf16 x bf16 into fp32).  Splitting P in
-// two bf16 terms keeps its relative error below 2^-18, so the result stays
-// within the stated tolerance of the exact definition even when few keys
-// carry the weight (P rounded once to bf16 or fp16 does not).
-//   warp 13     index resolution, up to eight tiles ahead: topk entry ->
-//               validity -> block_table -> physical row.
+// The stages follow "DeepSeek V3/V2 Sparse Flash Attention with Quantization",
+// section "Compute pipeline" (Sa_V0 gather + INT8 dequant, Sa_C1 S = Q K^T,
+// Sa_V1 softmax(S * scale), Sa_C2 O = P V, Sa_V2 O = o / l on the last tile)
+// with the running (m, l, o) update of its section "Flash online softmax
+// incremental update".
 //
-// The stages of the computation follow "DeepSeek V3/V2 Sparse Flash Attention
-// with Quantization", section "Compute pipeline": Sa_V0 gather (+ INT8
-// dequant), Sa_C1 S = Q K^T, Sa_V1 softmax(S * scale), Sa_C2 O = P V, Sa_V2
-// O = o / l on the last tile; the running (m, l, o) update is the one of the
-// section "Flash online softmax incremental update".
+// Precision: every product is exact (bf16 x bf16 into fp32).  P enters the
+// P.V product as two bf16 terms, so its relative error stays below 2^-18 and
+// the result meets the stated tolerance of the exact definition even when a
+// few keys carry the weight (P rounded once to bf16 or fp16 does not).
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <math.h>
-#include <stdint.h>
 #include <stdarg.h>
+#include <stdint.h>
 #include <stdio.h>
 #include <string.h>
 
@@ -51,53 +56,69 @@
 namespace mlasp {
 
 // ------------------------------------------------------------------ layout
-constexpr int kThreads = 448;
-constexpr int kGatherWarp0 = 4;
-constexpr int kMmaWarp = 12;
+constexpr int kThreads = 768;
+constexpr int kSoftmaxWarps = 8;
+constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
+constexpr int kSenderWarp0 = 8;
+constexpr int kSenderThreads = 128;
+constexpr int kGatherWarp0 = 12;
+constexpr int kMmaWarp = 20;
+constexpr int kIndexWarp = 21;
+// register shares (launch: 768 threads x 80 registers = 61,440)
+template <bool kInt8>
+struct Regs {
+  static constexpr uint32_t kSoftmax = kInt8 ? 120 : 136;
+  static constexpr uint32_t kGather = kInt8 ? 56 : 40;
+  static constexpr uint32_t kControl = 40;
+  static_assert(256 * kSoftmax + 128 * 80 + 256 * kGather + 128 * kControl <= 768 * 80, "register budget");
+};
+
 constexpr int kTileKeys = 64;
 constexpr int kStages = 4;
-constexpr int kIdxSlots = 8;
+constexpr int kIdxSlots = 4;
 constexpr int kHeads = 128;
-constexpr int kChunkBytes = kTileKeys * 128;   // 64 keys x 64 bf16 dims
-constexpr int kStageBytes = 5 * kChunkBytes;   // 4 latent chunks + 1 rope chunk
-constexpr int kRecvBytes = kHeads * kTileKeys * 4;
+constexpr int kChunkBytes = kTileKeys * 128;            // 64 keys x 64 bf16 latent dims (128-byte swizzle)
+constexpr int kRopeChunkBytes = kTileKeys * 64;         // 64 keys x 32 bf16 rope dims (64-byte swizzle)
+constexpr int kStageBytes = 4 * kChunkBytes + kRopeChunkBytes;
+constexpr int kRecvSlotBytes = kHeads * kTileKeys * 4;  // fp32 partial score tile
+constexpr int kQRopeBytes = kHeads * 64;
 
-constexpr int kQRopeBytes = kHeads * 128;     // Q rope half, 128-byte rows (64 B used)
-
-constexpr int kOffStages = 0;
-constexpr int kOffRecv = kOffStages + kStages * kStageBytes;
-constexpr int kOffQRope = kOffRecv + kRecvBytes;
-constexpr int kOffRows = kOffQRope + kQRopeBytes;                // int32 [kIdxSlots][64]
-constexpr int kOffVmask = kOffRows + kIdxSlots * kTileKeys * 4;  // uint16 [kStages][4]
-constexpr int kOffBars = kOffVmask + kStages * 4 * 2;
-// barrier indices
-constexpr int kBarFull = 0;                      // [kStages]
-constexpr int kBarEmpty = kBarFull + kStages;    // [kStages]
-constexpr int kBarIdxFull = kBarEmpty + kStages; // [kIdxSlots]
+constexpr int kOffRecv = 0;                             // same offset in both CTAs (peer writes here)
+constexpr int kOffStages = kOffRecv + 2 * kRecvSlotBytes;
+constexpr int kOffQRope = kOffStages + kStages * kStageBytes;
+constexpr int kOffRows = kOffQRope + kQRopeBytes;       // int32 [kIdxSlots][64]
+constexpr int kOffPair = kOffRows + kIdxSlots * kTileKeys * 4;
+constexpr int kOffVmask = kOffPair + 2 * kHeads * 4;    // uint64 [kStages]
+constexpr int kOffBars = kOffVmask + kStages * 8;
+constexpr int kBarFull = 0;
+constexpr int kBarEmpty = kBarFull + kStages;
+constexpr int kBarIdxFull = kBarEmpty + kStages;
 constexpr int kBarIdxEmpty = kBarIdxFull + kIdxSlots;
 constexpr int kBarSFull = kBarIdxEmpty + kIdxSlots;
 constexpr int kBarSFree = kBarSFull + 1;
 constexpr int kBarPFull = kBarSFree + 1;
 constexpr int kBarPvDone = kBarPFull + 1;
-constexpr int kBarRecvFull = kBarPvDone + 1;
-constexpr int kBarPeerFree = kBarRecvFull + 1;
-constexpr int kBarQReady = kBarPeerFree + 1;
+constexpr int kBarRecvFull = kBarPvDone + 1;   // [2]
+constexpr int kBarPeerFree = kBarRecvFull + 2;  // [2]
+constexpr int kBarPairA = kBarPeerFree + 2;     // [4]
+constexpr int kBarPairB = kBarPairA + 4;        // [4]
+constexpr int kBarQReady = kBarPairB + 4;
 constexpr int kBarFinal = kBarQReady + 1;
 constexpr int kNumBars = kBarFinal + 1;
 constexpr int kOffTmemSlot = kOffBars + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
-constexpr int kSmemUsed = kOffAbort + 4;
-constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
+constexpr int kSmemBytes = kOffAbort + 4;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kOffStages % 1024 == 0 && kStageBytes % 1024 == 0 && kOffQRope % 512 == 0, "operand alignment");
+static_assert(kOffBars % 8 == 0, "barrier alignment");
 
-// TMEM columns (512 allocated): O | S | P_hi | P_lo | Q latent (bf16 pairs)
+// TMEM columns (512 allocated): O | S | P_hi | P_lo | Q latent half (bf16 pairs)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;
 constexpr uint32_t kTmemS = 256;
 constexpr uint32_t kTmemPhi = 320;
 constexpr uint32_t kTmemPlo = 352;
 constexpr uint32_t kTmemQ = 384;
-static_assert(kTmemQ + 128 <= kTmemCols, "TMEM budget");
-static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;
 
@@ -119,11 +140,11 @@ struct Params {
 };
 
 struct Ctx {
-  uint32_t sbase;    // shared address of the aligned dynamic smem
-  uint8_t* smem;     // generic pointer to the same
-  uint32_t tmem;     // TMEM base
-  uint32_t crank;    // rank in the cluster (0/1)
-  int t;             // query token
+  uint32_t sbase;
+  uint8_t* smem;
+  uint32_t tmem;
+  uint32_t crank;
+  int t;
   volatile uint32_t* abort;
   __device__ uint32_t bar(int i) const { return sbase + kOffBars + 8 * i; }
 };
@@ -131,9 +152,8 @@ struct Ctx {
 __device__ __forceinline__ bool wait_bar(const Ctx& c, int idx, uint32_t parity) {
   return mbar_wait<false>(c.bar(idx), parity, c.abort, kWaitLimitNs);
 }
-// Warp-uniform variants: every lane waits (bounded) and the warp agrees on
-// the outcome, so warp-collective instructions after it never see a
-// partially departed warp.
+// Warp-uniform waits: every lane waits (bounded) and the warp agrees on the
+// outcome, so warp-collective instructions after it never see a partial warp.
 __device__ __forceinline__ bool warp_wait(const Ctx& c, int idx, uint32_t parity) {
   return __all_sync(0xffffffffu, wait_bar(c, idx, parity));
 }
@@ -142,7 +162,6 @@ __device__ __forceinline__ bool warp_wait_cluster(const Ctx& c, int idx, uint32_
 }
 
 __device__ __forceinline__ uint4 ldg16(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
-
 __device__ __forceinline__ void sts16(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
@@ -153,9 +172,13 @@ __device__ __forceinline__ float4 lds16f(uint32_t addr) {
                : "memory");
   return v;
 }
+// 16-byte unit u (0..15) of score row h in a receive slot, XOR-swizzled so a
+// warp's 32 rows spread over all banks.
+__device__ __forceinline__ uint32_t recv_unit(int h, int u) {
+  return static_cast<uint32_t>(h * 256 + ((u ^ (h & 15)) << 4));
+}
 
 // ------------------------------------------------------------------ index warp
-// Resolves topk entries of tiles [j0, j0+4) into physical row ids (-1: masked).
 __device__ void index_role(const Params& p, const Ctx& c, int lane) {
   const int b = c.t / p.S1;
   const int act = __ldg(p.act_seqs + b);
@@ -163,43 +186,50 @@ __device__ void index_role(const Params& p, const Ctx& c, int lane) {
   const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.mbps;
   int32_t* rows = reinterpret_cast<int32_t*>(c.smem + kOffRows);
   bool bad = false;
-  for (int j0 = 0; j0 < p.n_tiles; j0 += 4) {
-    const int nb = min(4, p.n_tiles - j0);
+  for (int j0 = 0; j0 < p.n_tiles; j0 += 2) {
+    const int nb = min(2, p.n_tiles - j0);
     bool ok = true;
     for (int k = 0; k < nb && ok; ++k) {
       const int j = j0 + k;
-      ok = warp_wait(c, kBarIdxEmpty + (j & (kIdxSlots - 1)), ((j >> 3) & 1) ^ 1);
+      ok = warp_wait(c, kBarIdxEmpty + (j % kIdxSlots), ((j / kIdxSlots) & 1) ^ 1);
     }
     if (!ok) break;
-    int idx[8], blk[8];
+    int idx[4], blk[4];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
+    for (int q = 0; q < 4; ++q) {
       const int e = (j0 + (q >> 1)) * kTileKeys + (q & 1) * 32 + lane;
       idx[q] = ((q >> 1) < nb && e < p.topk) ? __ldg(tk + e) : -1;
     }
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
+    for (int q = 0; q < 4; ++q) {
       const bool valid = idx[q] >= 0 && idx[q] < act;
       const int slot = idx[q] >> 7;
       blk[q] = (valid && slot < p.mbps) ? __ldg(bt + slot) : -1;
       if (valid && (blk[q] < 0 || blk[q] >= p.num_blocks)) bad = true;
     }
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
+    for (int q = 0; q < 4; ++q) {
       if ((q >> 1) >= nb) continue;
       const bool valid = idx[q] >= 0 && idx[q] < act && blk[q] >= 0 && blk[q] < p.num_blocks;
       const int j = j0 + (q >> 1);
-      rows[(j & (kIdxSlots - 1)) * kTileKeys + (q & 1) * 32 + lane] = valid ? (blk[q] * 128 + (idx[q] & 127)) : -1;
+      rows[(j % kIdxSlots) * kTileKeys + (q & 1) * 32 + lane] = valid ? (blk[q] * 128 + (idx[q] & 127)) : -1;
     }
-    for (int k = 0; k < nb; ++k) mbar_arrive(c.bar(kBarIdxFull + ((j0 + k) & (kIdxSlots - 1))));
+    for (int k = 0; k < nb; ++k) mbar_arrive(c.bar(kBarIdxFull + ((j0 + k) % kIdxSlots)));
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&g_mla_status, MLA_DEVICE_BAD_BLOCK);
 }
 
 // ------------------------------------------------------------------ gather warps
-// Dequantise 4 int8 values (one word) with one fp32 scale: bf16(fp32(q) * s),
-// as two bf16x2 words ("INT8 quantization path": INT8 -> FP16 -> FP32, times
-// the group scale, -> BF16; the INT8 -> FP32 widening is exact).
+// Stage layout (per 64-key tile): chunks 0-3 hold this CTA's latent dims
+// [64c, 64c+64) in 128-byte rows (unit u of key k at u ^ (k & 7)); the rope
+// chunk holds this CTA's 32 rope dims in 64-byte rows (unit u of key k at
+// u ^ ((k >> 1) & 3)).
+__device__ __forceinline__ uint32_t rope_unit(int k, int u) {
+  return static_cast<uint32_t>(k * 64 + ((u ^ ((k >> 1) & 3)) << 4));
+}
+
+// INT8 path: "INT8 quantization path" -- INT8 -> FP16 -> FP32 (exact), times
+// the group scale (one fp32 rounding), -> BF16.
 __device__ __forceinline__ void dequant4(uint32_t w, float s, uint32_t& lo, uint32_t& hi) {
   const float f0 = __fmul_rn(__int2float_rn(static_cast<int>(w << 24) >> 24), s);
   const float f1 = __fmul_rn(__int2float_rn(static_cast<int>(w << 16) >> 24), s);
@@ -209,55 +239,48 @@ __device__ __forceinline__ void dequant4(uint32_t w, float s, uint32_t& lo, uint
   hi = pack_bf16x2(f2, f3);
 }
 
-// Stage layout (per 64-key tile): chunks 0-3 hold latent dims [64c, 64c+64)
-// of this CTA's half, chunk 4 the rope half in the first 64 bytes of each
-// 128-byte row; row = key, 16-byte unit u of row k stored at unit u ^ (k & 7).
 template <bool kInt8>
 __device__ void gather_role(const Params& p, const Ctx& c, int gw, int lane) {
-  const int g = gw >> 2;   // tile parity handled by this group
-  const int w4 = gw & 3;   // warp within the group: keys [16*w4, 16*w4+16)
-  const int32_t* rows_all = reinterpret_cast<const int32_t*>(c.smem + kOffRows);
-  uint16_t* vmask = reinterpret_cast<uint16_t*>(c.smem + kOffVmask);
-  const uint8_t* kv_rope = reinterpret_cast<const uint8_t*>(p.kv_rope);
+  const int g = gw >> 2;  // tiles j with j % 2 == g
+  const int w4 = gw & 3;  // keys [16 w4, 16 w4 + 16)
   const int key0 = w4 * 16;
-  const int ru = lane & 3;
+  const int32_t* rows_all = reinterpret_cast<const int32_t*>(c.smem + kOffRows);
+  uint16_t* vmask16 = reinterpret_cast<uint16_t*>(c.smem + kOffVmask);
+  const uint8_t* kvr = reinterpret_cast<const uint8_t*>(p.kv_rope) + c.crank * 64 + (lane & 3) * 16;
+  const int rk0 = key0 + (lane >> 2), rk1 = key0 + 8 + (lane >> 2);
   for (int j = g; j < p.n_tiles; j += 2) {
-    const int st = j & (kStages - 1);
-    const int slot = j & (kIdxSlots - 1);
-    if (!warp_wait(c, kBarEmpty + st, ((j >> 2) & 1) ^ 1)) break;
-    if (!warp_wait(c, kBarIdxFull + slot, (j >> 3) & 1)) break;
-    const int32_t* rows = rows_all + slot * kTileKeys + key0;
-    int32_t myrow[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) myrow[i] = rows[i];
-    const int32_t rope_row0 = rows[lane >> 2];
-    const int32_t rope_row1 = rows[8 + (lane >> 2)];
-    const uint32_t vbits = __ballot_sync(0xffffffffu, lane < 16 && rows[lane & 15] >= 0) & 0xFFFFu;
-    mbar_arrive(c.bar(kBarIdxEmpty + slot));
+    const int st = j % kStages;
+    const int slot = j % kIdxSlots;
+    if (!warp_wait(c, kBarEmpty + st, ((j / kStages) & 1) ^ 1)) break;
+    if (!warp_wait(c, kBarIdxFull + slot, (j / kIdxSlots) & 1)) break;
+    const int32_t* rows = rows_all + slot * kTileKeys;
+    const uint32_t vbits = __ballot_sync(0xffffffffu, lane < 16 && rows[key0 + (lane & 15)] >= 0) & 0xFFFFu;
+    const int32_t r0 = rows[rk0], r1 = rows[rk1];
     const uint32_t stage = c.sbase + kOffStages + st * kStageBytes;
-    const uint32_t rope_chunk = stage + 4 * kChunkBytes;
-    const int k0 = key0 + (lane >> 2), k1 = key0 + 8 + (lane >> 2);
+    const uint32_t rope = stage + 4 * kChunkBytes;
     if constexpr (!kInt8) {
-      // latent half: 512 B per key = 32 lanes x 16 B, one row per warp instruction
+      // latent half: 512 B per key, one key per warp instruction (32 lanes x 16 B)
       const uint8_t* kvn = reinterpret_cast<const uint8_t*>(p.kv_nope) + c.crank * 512 + lane * 16;
       const uint32_t chunk = stage + (lane >> 3) * kChunkBytes;
-#pragma unroll
+#pragma unroll 4
       for (int i = 0; i < 16; ++i) {
         const int key = key0 + i;
-        const int32_t row = myrow[i];
+        const int32_t row = rows[key];
         cp_async_16(chunk + key * 128 + (((lane & 7) ^ (key & 7)) << 4),
                     row >= 0 ? kvn + static_cast<int64_t>(row) * 1024 : kvn, row >= 0 ? 16u : 0u);
       }
-      const uint8_t* kvr = kv_rope + c.crank * 64 + ru * 16;
-      cp_async_16(rope_chunk + k0 * 128 + ((ru ^ (k0 & 7)) << 4),
-                  rope_row0 >= 0 ? kvr + static_cast<int64_t>(rope_row0) * 128 : kvr, rope_row0 >= 0 ? 16u : 0u);
-      cp_async_16(rope_chunk + k1 * 128 + ((ru ^ (k1 & 7)) << 4),
-                  rope_row1 >= 0 ? kvr + static_cast<int64_t>(rope_row1) * 128 : kvr, rope_row1 >= 0 ? 16u : 0u);
+      cp_async_16(rope + rope_unit(rk0, lane & 3), r0 >= 0 ? kvr + static_cast<int64_t>(r0) * 128 : kvr,
+                  r0 >= 0 ? 16u : 0u);
+      cp_async_16(rope + rope_unit(rk1, lane & 3), r1 >= 0 ? kvr + static_cast<int64_t>(r1) * 128 : kvr,
+                  r1 >= 0 ? 16u : 0u);
+      mbar_arrive_relaxed(c.bar(kBarIdxEmpty + slot));
       cp_async_arrive_noinc(c.bar(kBarFull + st));
+      if (lane == 0) {
+        vmask16[st * 4 + w4] = static_cast<uint16_t>(vbits);
+        mbar_arrive(c.bar(kBarFull + st));  // releases the mask word
+      }
     } else {
       const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-      const uint4 r0 = rope_row0 >= 0 ? ldg16(kv_rope + static_cast<int64_t>(rope_row0) * 128 + c.crank * 64 + ru * 16) : zero;
-      const uint4 r1 = rope_row1 >= 0 ? ldg16(kv_rope + static_cast<int64_t>(rope_row1) * 128 + c.crank * 64 + ru * 16) : zero;
       // latent half: 256 int8 per key = 16 lanes x 16 B; lanes 16-31 take the next key
       const int u = lane & 15;
       const int8_t* kvn = reinterpret_cast<const int8_t*>(p.kv_nope) + c.crank * 256 + u * 16;
@@ -266,12 +289,15 @@ __device__ void gather_role(const Params& p, const Ctx& c, int gw, int lane) {
       float sc[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const int32_t row = rows[2 * i + (lane >> 4)];
+        const int32_t row = rows[key0 + 2 * i + (lane >> 4)];
         v[i] = row >= 0 ? ldg16(kvn + static_cast<int64_t>(row) * 512) : zero;
         sc[i] = row >= 0 ? __ldg(scl + static_cast<int64_t>(row) * 4) : 0.f;
       }
+      const uint4 q0 = r0 >= 0 ? ldg16(kvr + static_cast<int64_t>(r0) * 128) : zero;
+      const uint4 q1 = r1 >= 0 ? ldg16(kvr + static_cast<int64_t>(r1) * 128) : zero;
+      mbar_arrive_relaxed(c.bar(kBarIdxEmpty + slot));
       const uint32_t chunk = stage + (u >> 2) * kChunkBytes;
-      const int u8 = (u & 3) * 2;  // first 8-element unit of these 16 dims within the chunk
+      const int u8 = (u & 3) * 2;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int key = key0 + 2 * i + (lane >> 4);
@@ -283,15 +309,46 @@ __device__ void gather_role(const Params& p, const Ctx& c, int gw, int lane) {
         sts16(chunk + key * 128 + ((u8 ^ (key & 7)) << 4), a);
         sts16(chunk + key * 128 + (((u8 + 1) ^ (key & 7)) << 4), b2);
       }
-      sts16(rope_chunk + k0 * 128 + ((ru ^ (k0 & 7)) << 4), r0);
-      sts16(rope_chunk + k1 * 128 + ((ru ^ (k1 & 7)) << 4), r1);
+      sts16(rope + rope_unit(rk0, lane & 3), q0);
+      sts16(rope + rope_unit(rk1, lane & 3), q1);
+      if (lane == 0) vmask16[st * 4 + w4] = static_cast<uint16_t>(vbits);
       fence_proxy_async_smem();
       mbar_arrive(c.bar(kBarFull + st));
     }
-    if (lane == 0) {
-      vmask[st * 4 + w4] = static_cast<uint16_t>(vbits);
-      mbar_arrive(c.bar(kBarFull + st));  // releases the mask word
+  }
+}
+
+// ------------------------------------------------------------------ sender warps
+// Push the CTA's partial score tile (128 heads x 64 keys, fp32) to the peer.
+__device__ void sender_role(const Params& p, const Ctx& c, int q, int lane) {
+  const int h = q * 32 + lane;
+  const uint32_t tS = c.tmem + (static_cast<uint32_t>(q * 32) << 16) + kTmemS;
+  const uint32_t peer = c.crank ^ 1u;
+  const uint32_t recv_remote = mapa_shared(c.sbase + kOffRecv, peer);
+  for (int j = 0; j < p.n_tiles; ++j) {
+    if (!warp_wait(c, kBarSFull, j & 1)) break;
+    tc_fence_after();
+    uint32_t r[64];
+    {
+      uint32_t a[32], b[32];
+      tmem_ld_32x32b_x32(tS, a);
+      tmem_ld_32x32b_x32(tS + 32, b);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        r[i] = a[i];
+        r[32 + i] = b[i];
+      }
     }
+    tc_fence_before();
+    mbar_arrive_relaxed(c.bar(kBarSFree));  // the values are in registers (wait::ld)
+    const int b = j & 1;
+    if (j >= 2 && !warp_wait_cluster(c, kBarPeerFree + b, ((j >> 1) & 1) ^ 1)) break;
+    const uint32_t dst = recv_remote + b * kRecvSlotBytes;
+    const uint32_t rbar = mapa_shared(c.bar(kBarRecvFull + b), peer);
+#pragma unroll
+    for (int u = 0; u < 16; ++u)
+      st_async_v4(dst + recv_unit(h, u), r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3], rbar);
   }
 }
 
@@ -300,15 +357,15 @@ __device__ __forceinline__ bool issue_pv(const Ctx& c, int i) {
   if (!wait_bar(c, kBarPFull, i & 1)) return false;
   tc_fence_after();
   constexpr uint32_t idesc = make_idesc_f16(128, 256, 1, 0, 1);
-  const uint32_t stage = c.sbase + kOffStages + (i & (kStages - 1)) * kStageBytes;
-  // O += P_hi . V, then O += P_lo . V (same V tile, K = 16 keys per instruction)
+  const uint32_t stage = c.sbase + kOffStages + (i % kStages) * kStageBytes;
+  // O += P_hi . V, then O += P_lo . V (same V tile, 16 keys per instruction)
 #pragma unroll
   for (int s = 0; s < 8; ++s)
     umma_ts(c.tmem + kTmemO, c.tmem + (s < 4 ? kTmemPhi : kTmemPlo) + 8 * (s & 3),
             make_sdesc(stage + (s & 3) * 16 * 128, kChunkBytes, 1024, kSwizzle128B), idesc,
             (i > 0 || s > 0) ? 1u : 0u);
   umma_commit(c.bar(kBarPvDone));
-  umma_commit(c.bar(kBarEmpty + (i & (kStages - 1))));
+  umma_commit(c.bar(kBarEmpty + (i % kStages)));
   return true;
 }
 
@@ -316,28 +373,28 @@ __device__ void mma_role(const Params& p, const Ctx& c) {
   constexpr uint32_t idesc_s = make_idesc_f16(128, 64, 1, 0, 0);
   const uint32_t qrope = c.sbase + kOffQRope;
   bool ok = wait_bar(c, kBarQReady, 0);
-  int j = 0;
-  for (; ok && j < p.n_tiles; ++j) {
-    const int st = j & (kStages - 1);
-    if (!wait_bar(c, kBarFull + st, (j >> 2) & 1)) { ok = false; break; }
-    if (j > 0 && !wait_bar(c, kBarSFree, (j - 1) & 1)) { ok = false; break; }
-    fence_proxy_async_smem();  // cp.async data (generic proxy) -> tensor-core reads
-    tc_fence_after();
-    const uint32_t stage = c.sbase + kOffStages + st * kStageBytes;
+  // Issue order S(k), P.V(k-2): the softmax runs one tile behind the score MMA.
+  for (int k = 0; ok && k < p.n_tiles + 2; ++k) {
+    if (k < p.n_tiles) {
+      const int st = k % kStages;
+      if (!wait_bar(c, kBarFull + st, (k / kStages) & 1)) { ok = false; break; }
+      if (k > 0 && !wait_bar(c, kBarSFree, (k - 1) & 1)) { ok = false; break; }
+      fence_proxy_async_smem();  // cp.async / st.shared data -> tensor-core reads
+      tc_fence_after();
+      const uint32_t stage = c.sbase + kOffStages + st * kStageBytes;
 #pragma unroll
-    for (int s = 0; s < 16; ++s)
-      umma_ts(c.tmem + kTmemS, c.tmem + kTmemQ + 8 * s,
-              make_sdesc(stage + (s >> 2) * kChunkBytes + (s & 3) * 32, 16, 1024, kSwizzle128B), idesc_s,
-              s > 0 ? 1u : 0u);
+      for (int s = 0; s < 16; ++s)
+        umma_ts(c.tmem + kTmemS, c.tmem + kTmemQ + 8 * s,
+                make_sdesc(stage + (s >> 2) * kChunkBytes + (s & 3) * 32, 16, 1024, kSwizzle128B), idesc_s,
+                s > 0 ? 1u : 0u);
 #pragma unroll
-    for (int s = 0; s < 2; ++s)
-      umma_ss(c.tmem + kTmemS, make_sdesc(qrope + s * 32, 16, 1024, kSwizzle128B),
-              make_sdesc(stage + 4 * kChunkBytes + s * 32, 16, 1024, kSwizzle128B), idesc_s, 1u);
-    umma_commit(c.bar(kBarSFull));
-    if (j > 0 && !issue_pv(c, j - 1)) { ok = false; break; }
+      for (int s = 0; s < 2; ++s)
+        umma_ss(c.tmem + kTmemS, make_sdesc(qrope + s * 32, 16, 512, kSwizzle64B),
+                make_sdesc(stage + 4 * kChunkBytes + s * 32, 16, 512, kSwizzle64B), idesc_s, 1u);
+      umma_commit(c.bar(kBarSFull));
+    }
+    if (k >= 2 && !issue_pv(c, k - 2)) { ok = false; break; }
   }
-  if (ok) issue_pv(c, p.n_tiles - 1);
-  // Drain: every MMA issued above must finish before TMEM is released.
   umma_commit(c.bar(kBarFinal));
   volatile uint32_t never = 0;
   mbar_wait<false>(c.bar(kBarFinal), 0, &never, kWaitLimitNs);
@@ -345,22 +402,24 @@ __device__ void mma_role(const Params& p, const Ctx& c) {
 
 // ------------------------------------------------------------------ softmax warps
 __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) {
-  const int h = warp * 32 + lane;
-  const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-  const uint32_t tS = c.tmem + lane_off + kTmemS;
-  const uint32_t tPhi = c.tmem + lane_off + kTmemPhi;
-  const uint32_t tPlo = c.tmem + lane_off + kTmemPlo;
-  const uint32_t tO = c.tmem + lane_off + kTmemO;
-  const uint32_t tQ = c.tmem + lane_off + kTmemQ;
+  const int q = warp & 3;          // TMEM lane quadrant
+  const int half = warp >> 2;      // key columns [32 half, 32 half + 32)
+  const int h = q * 32 + lane;     // head
+  const int tid = warp * 32 + lane;
+  const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+  const uint32_t tS = c.tmem + lane_off + kTmemS + 32 * half;
+  const uint32_t tPhi = c.tmem + lane_off + kTmemPhi + 16 * half;
+  const uint32_t tPlo = c.tmem + lane_off + kTmemPlo + 16 * half;
+  const uint32_t tO = c.tmem + lane_off + kTmemO + 128 * half;
+  const uint32_t tQ = c.tmem + lane_off + kTmemQ + 64 * half;
   const bool live = h < p.n_q;
   const int64_t qrow = static_cast<int64_t>(c.t) * p.n_q + h;
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  // Q half row: latent part (bf16 pairs) -> TMEM lane h, rope part -> shared
-  // memory row h (the A operand of the two rope MMA steps).
   {
-    const uint8_t* qn = reinterpret_cast<const uint8_t*>(p.q_nope) + (qrow * 512 + c.crank * 256) * 2;
+    // Q latent: this thread stores dims [128 half, 128 half + 128) of the CTA's 256
+    const uint8_t* qn = reinterpret_cast<const uint8_t*>(p.q_nope) + (qrow * 512 + c.crank * 256 + half * 128) * 2;
 #pragma unroll
-    for (int ch = 0; ch < 4; ++ch) {
+    for (int ch = 0; ch < 2; ++ch) {
       uint32_t w[32];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -372,12 +431,12 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
       }
       tmem_st_32x32b_x32(tQ + 32 * ch, w);
     }
-    const uint8_t* qr = reinterpret_cast<const uint8_t*>(p.q_rope) + (qrow * 64 + c.crank * 32) * 2;
-    const uint32_t qrope_row = c.sbase + kOffQRope + h * 128;
+    // Q rope: this CTA's 32 dims [32 crank, 32 crank + 32), units 2 half, 2 half + 1
+    const uint8_t* qr = reinterpret_cast<const uint8_t*>(p.q_rope) + (qrow * 64 + c.crank * 32 + half * 16) * 2;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 2; ++u) {
       const uint4 v = live ? ldg16(qr + u * 16) : zero;
-      sts16(qrope_row + ((u ^ (h & 7)) << 4), v);
+      sts16(c.sbase + kOffQRope + rope_unit(h, 2 * half + u), v);
     }
     fence_proxy_async_smem();
     tmem_wait_st();
@@ -385,106 +444,120 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
     mbar_arrive(c.bar(kBarQReady));
   }
   const uint32_t peer = c.crank ^ 1u;
-  const uint32_t recv_local = c.sbase + kOffRecv + h * 256;
-  const uint32_t recv_remote = mapa_shared(recv_local, peer);
-  const uint32_t recv_full_remote = mapa_shared(c.bar(kBarRecvFull), peer);
-  const uint32_t peer_free_remote = mapa_shared(c.bar(kBarPeerFree), peer);
-  const uint32_t sw = static_cast<uint32_t>(h & 15);
-  const uint16_t* vmask = reinterpret_cast<const uint16_t*>(c.smem + kOffVmask);
+  float* pair = reinterpret_cast<float*>(c.smem + kOffPair);
+  const uint64_t* vmask = reinterpret_cast<const uint64_t*>(c.smem + kOffVmask);
   const float scl = p.scale_log2;
   float m = -INFINITY, l = 0.f;
+  float own_prev[32];
   bool ok = true;
-  for (int j = 0; j < p.n_tiles; ++j) {
-    if (!warp_wait(c, kBarSFull, j & 1)) { ok = false; break; }
-    tc_fence_after();
-    uint32_t r[64];
-    tmem_ld_32x32b_x64(tS, r);
-    tmem_wait_ld();
-    tc_fence_before();
-    mbar_arrive(c.bar(kBarSFree));
-    // exchange partial scores with the peer CTA
-    if (j > 0 && !warp_wait_cluster(c, kBarPeerFree, (j - 1) & 1)) { ok = false; break; }
-#pragma unroll
-    for (int u = 0; u < 16; ++u)
-      st_async_v4(recv_remote + ((u ^ sw) << 4), r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3], recv_full_remote);
-    if (!warp_wait_cluster(c, kBarRecvFull, j & 1)) { ok = false; break; }
-    if (h == 0 && j + 1 < p.n_tiles) mbar_arrive_expect_tx(c.bar(kBarRecvFull), kRecvBytes);
-    float s[64];
-#pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      const float4 v = lds16f(recv_local + ((u ^ sw) << 4));
-      s[4 * u + 0] = __uint_as_float(r[4 * u + 0]) + v.x;
-      s[4 * u + 1] = __uint_as_float(r[4 * u + 1]) + v.y;
-      s[4 * u + 2] = __uint_as_float(r[4 * u + 2]) + v.z;
-      s[4 * u + 3] = __uint_as_float(r[4 * u + 3]) + v.w;
-    }
-    mbar_arrive_remote(peer_free_remote);
-    // validity of the tile's 64 entries (acquire the gather's writes)
-    if (!warp_wait(c, kBarFull + (j & (kStages - 1)), (j >> 2) & 1)) { ok = false; break; }
-    const uint16_t* vm16 = vmask + (j & (kStages - 1)) * 4;
-    const uint64_t vm = static_cast<uint64_t>(vm16[0]) | (static_cast<uint64_t>(vm16[1]) << 16) |
-                        (static_cast<uint64_t>(vm16[2]) << 32) | (static_cast<uint64_t>(vm16[3]) << 48);
-    float mx = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < 64; ++i) {
-      s[i] = ((vm >> i) & 1ull) ? s[i] * scl : -INFINITY;
-      mx = fmaxf(mx, s[i]);
-    }
-    // Lazy rescale: the running max m only moves when a head's tile max exceeds
-    // it by more than 8 (log2 units), so P stays <= 2^8 and O is rescaled rarely.
-    const bool grow = mx > m + 8.f;
-    const float f = grow ? fast_exp2(m - mx) : 1.f;  // m = -inf -> 0
-    if (grow) {
-      l *= f;
-      m = mx;
-    }
-    if (__any_sync(0xffffffffu, grow) && j > 0) {
-      // TMEM accesses are warp-collective: the whole warp waits for the previous
-      // P.V, then every lane rescales its own O row (f = 1 where m did not move).
-      if (!warp_wait(c, kBarPvDone, (j - 1) & 1)) { ok = false; break; }
+  for (int j = 0; j <= p.n_tiles; ++j) {
+    float own_cur[32];
+    if (j < p.n_tiles) {
+      // own partial score tile j (kept until the peer's partial arrives)
+      if (!warp_wait(c, kBarSFull, j & 1)) { ok = false; break; }
       tc_fence_after();
-#pragma unroll 1
-      for (int ch = 0; ch < 16; ++ch) {
-        uint32_t o[16];
-        tmem_ld_32x32b_x16(tO + 16 * ch, o);
-        tmem_wait_ld();
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(tS, r);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive_relaxed(c.bar(kBarSFree));
 #pragma unroll
-        for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-        tmem_st_32x32b_x16(tO + 16 * ch, o);
+      for (int i = 0; i < 32; ++i) own_cur[i] = __uint_as_float(r[i]);
+    }
+    if (j >= 1) {
+      const int i = j - 1;  // tile whose softmax runs now
+      const int b = i & 1;
+      if (!warp_wait_cluster(c, kBarRecvFull + b, (i >> 1) & 1)) { ok = false; break; }
+      if (tid == 0 && i + 2 < p.n_tiles) mbar_arrive_expect_tx(c.bar(kBarRecvFull + b), kRecvSlotBytes);
+      float s[32];
+      const uint32_t slot = c.sbase + kOffRecv + b * kRecvSlotBytes;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float4 v = lds16f(slot + recv_unit(h, 8 * half + k));
+        s[4 * k + 0] = own_prev[4 * k + 0] + v.x;
+        s[4 * k + 1] = own_prev[4 * k + 1] + v.y;
+        s[4 * k + 2] = own_prev[4 * k + 2] + v.z;
+        s[4 * k + 3] = own_prev[4 * k + 3] + v.w;
       }
-      tmem_wait_st();
-    }
-    const float mm = (m == -INFINITY) ? 0.f : m;
-    uint32_t phi[32], plo[32];
-    float lsum = 0.f;
+      mbar_arrive_remote_relaxed(mapa_shared(c.bar(kBarPeerFree + b), peer));  // the values were consumed
+      // mask (waiting on the stage barrier acquires the gather's validity bits) and scale
+      if (!warp_wait(c, kBarFull + (i % kStages), (i / kStages) & 1)) { ok = false; break; }
+      const uint32_t vm = static_cast<uint32_t>(vmask[i % kStages] >> (32 * half));
+      float mx = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float p0 = fast_exp2(s[2 * i] - mm);
-      const float p1 = fast_exp2(s[2 * i + 1] - mm);
-      lsum += p0 + p1;
-      const uint32_t hw = pack_bf16x2(p0, p1);
-      phi[i] = hw;
-      // p - bf16(p) is exact in fp32; its bf16 rounding leaves an error <= 2^-18 p
-      plo[i] = pack_bf16x2(p0 - __uint_as_float(hw << 16), p1 - __uint_as_float(hw & 0xFFFF0000u));
+      for (int k = 0; k < 32; ++k) {
+        s[k] = ((vm >> k) & 1u) ? s[k] * scl : -INFINITY;
+        mx = fmaxf(mx, s[k]);
+      }
+      // row max across the two column halves of head h (bounded handshake
+      // between warps q and q + 4: post, both posted, read, both read)
+      pair[half * kHeads + h] = mx;
+      mbar_arrive(c.bar(kBarPairA + q));
+      if (!warp_wait(c, kBarPairA + q, i & 1)) { ok = false; break; }
+      mx = fmaxf(mx, pair[(half ^ 1) * kHeads + h]);
+      mbar_arrive(c.bar(kBarPairB + q));
+      if (!warp_wait(c, kBarPairB + q, i & 1)) { ok = false; break; }
+      // Lazy rescale: m only moves when the tile max exceeds it by more than 8
+      // (log2 units), so P stays below 2^8 and O is rescaled rarely.
+      const bool grow = mx > m + 8.f;
+      const float f = grow ? fast_exp2(m - mx) : 1.f;  // m = -inf -> 0
+      if (grow) {
+        l *= f;
+        m = mx;
+      }
+      if (__any_sync(0xffffffffu, grow) && i > 0) {
+        if (!warp_wait(c, kBarPvDone, (i - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(tO + 32 * ch, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
+          tmem_st_32x32b_x32(tO + 32 * ch, o);
+        }
+        tmem_wait_st();
+      }
+      const float mm = (m == -INFINITY) ? 0.f : m;
+      uint32_t phi[16], plo[16];
+      float lsum = 0.f;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float p0 = fast_exp2(s[2 * k] - mm);
+        const float p1 = fast_exp2(s[2 * k + 1] - mm);
+        lsum += p0 + p1;
+        const uint32_t hw = pack_bf16x2(p0, p1);
+        phi[k] = hw;
+        // p - bf16(p) is exact in fp32; its bf16 rounding leaves an error <= 2^-18 p
+        plo[k] = pack_bf16x2(p0 - __uint_as_float(hw << 16), p1 - __uint_as_float(hw & 0xFFFF0000u));
+      }
+      l += lsum;
+      if (i > 0) {
+        if (!warp_wait(c, kBarPvDone, (i - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+      }
+      tmem_st_32x32b_x16(tPhi, phi);
+      tmem_st_32x32b_x16(tPlo, plo);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(c.bar(kBarPFull));
     }
-    l += lsum;
-    if (j > 0) {
-      if (!warp_wait(c, kBarPvDone, (j - 1) & 1)) { ok = false; break; }
-      tc_fence_after();
-    }
-    tmem_st_32x32b_x32(tPhi, phi);
-    tmem_st_32x32b_x32(tPlo, plo);
-    tmem_wait_st();
-    tc_fence_before();
-    mbar_arrive(c.bar(kBarPFull));
+#pragma unroll
+    for (int k = 0; k < 32; ++k) own_prev[k] = own_cur[k];
   }
   if (!ok) return;
+  // l over the whole row: add the partner's column half (same order in both threads)
+  pair[half * kHeads + h] = l;
+  mbar_arrive(c.bar(kBarPairA + q));
+  if (!warp_wait(c, kBarPairA + q, p.n_tiles & 1)) return;
+  const float l_tot = half == 0 ? l + pair[kHeads + h] : pair[h] + l;
   if (!warp_wait(c, kBarPvDone, (p.n_tiles - 1) & 1)) return;
   tc_fence_after();
-  const float inv_l = l > 0.f ? 1.f / l : 0.f;
-  uint4* op = reinterpret_cast<uint4*>(p.out + qrow * 512 + c.crank * 256);
+  const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
+  uint4* op = reinterpret_cast<uint4*>(p.out + qrow * 512 + c.crank * 256 + half * 128);
 #pragma unroll 1
-  for (int ch = 0; ch < 8; ++ch) {
+  for (int ch = 0; ch < 4; ++ch) {
     uint32_t o[32];
     tmem_ld_32x32b_x32(tO + 32 * ch, o);
     tmem_wait_ld();
@@ -500,15 +573,14 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
       }
     }
   }
-  if (live && c.crank == 0 && p.lse != nullptr)
-    p.lse[qrow] = l > 0.f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+  if (live && c.crank == 0 && half == 0 && p.lse != nullptr)
+    p.lse[qrow] = l_tot > 0.f ? (m + log2f(l_tot)) * 0.69314718055994530942f : -INFINITY;
 }
 
 // ------------------------------------------------------------------ kernel
 template <bool kInt8>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_sparse_fwd_kernel(const Params p) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_sparse_fwd_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   Ctx c;
   c.smem = smem;
@@ -517,9 +589,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_spa
   c.t = blockIdx.x >> 1;
   c.abort = reinterpret_cast<volatile uint32_t*>(smem + kOffAbort);
   if (tid == 0) {
-    *c.abort = (*reinterpret_cast<volatile unsigned int*>(&g_mla_status) & MLA_DEVICE_TIMEOUT) ? 1u : 0u;
+    // the swizzled operand layouts need a 1024-byte aligned base
+    const bool misaligned = (c.sbase & 1023u) != 0;
+    *c.abort = ((*reinterpret_cast<volatile unsigned int*>(&g_mla_status) & MLA_DEVICE_TIMEOUT) || misaligned) ? 1u : 0u;
+    if (misaligned) atomicOr(&g_mla_status, MLA_DEVICE_TIMEOUT);
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(c.bar(kBarFull + i), 128 + 4);
+      mbar_init(c.bar(kBarFull + i), kInt8 ? 128 : 128 + 4);
       mbar_init(c.bar(kBarEmpty + i), 1);
     }
     for (int i = 0; i < kIdxSlots; ++i) {
@@ -527,15 +602,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_spa
       mbar_init(c.bar(kBarIdxEmpty + i), 128);
     }
     mbar_init(c.bar(kBarSFull), 1);
-    mbar_init(c.bar(kBarSFree), 128);
-    mbar_init(c.bar(kBarPFull), 128);
+    mbar_init(c.bar(kBarSFree), kSoftmaxThreads + kSenderThreads);
+    mbar_init(c.bar(kBarPFull), kSoftmaxThreads);
     mbar_init(c.bar(kBarPvDone), 1);
-    mbar_init(c.bar(kBarRecvFull), 1);
-    mbar_init(c.bar(kBarPeerFree), 128);
-    mbar_init(c.bar(kBarQReady), 128);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(c.bar(kBarRecvFull + b), 1);
+      mbar_init(c.bar(kBarPeerFree + b), kSoftmaxThreads);
+    }
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(c.bar(kBarPairA + q), 64);
+      mbar_init(c.bar(kBarPairB + q), 64);
+    }
+    mbar_init(c.bar(kBarQReady), kSoftmaxThreads);
     mbar_init(c.bar(kBarFinal), 1);
     fence_mbarrier_init_cluster();
-    mbar_arrive_expect_tx(c.bar(kBarRecvFull), kRecvBytes);  // phase 0 of the score exchange
+    for (int b = 0; b < 2; ++b) mbar_arrive_expect_tx(c.bar(kBarRecvFull + b), kRecvSlotBytes);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(c.sbase + kOffTmemSlot, kTmemCols);
@@ -547,16 +628,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_spa
   tc_fence_after();
   c.tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmemSlot);
 
-  if (!*c.abort) {
-    if (warp < kGatherWarp0) {
-      softmax_role(p, c, warp, lane);
-    } else if (warp < kMmaWarp) {
-      gather_role<kInt8>(p, c, warp - kGatherWarp0, lane);
-    } else if (warp == kMmaWarp) {
-      if (lane == 0) mma_role(p, c);
-      __syncwarp();
-    } else {
-      index_role(p, c, lane);
+  if (warp < kSenderWarp0) {
+    regs_increase<Regs<kInt8>::kSoftmax>();
+    if (!*c.abort) softmax_role(p, c, warp, lane);
+  } else if (warp < kGatherWarp0) {
+    if (!*c.abort) sender_role(p, c, warp - kSenderWarp0, lane);
+  } else if (warp < kMmaWarp) {
+    regs_decrease<Regs<kInt8>::kGather>();
+    if (!*c.abort) gather_role<kInt8>(p, c, warp - kGatherWarp0, lane);
+  } else {
+    regs_decrease<Regs<kInt8>::kControl>();
+    if (!*c.abort) {
+      if (warp == kMmaWarp) {
+        if (lane == 0) mma_role(p, c);
+        __syncwarp();
+      } else if (warp == kIndexWarp) {
+        index_role(p, c, lane);
+      }
     }
   }
 
@@ -595,8 +683,19 @@ cudaError_t g_attr_err[kMaxDevices][2];
 template <bool kInt8>
 cudaError_t prepare_kernel(int dev) {
   std::call_once(g_attr_once[dev][kInt8 ? 1 : 0], [dev] {
-    g_attr_err[dev][kInt8 ? 1 : 0] = cudaFuncSetAttribute(
-        mlasp::mla_sparse_fwd_kernel<kInt8>, cudaFuncAttributeMaxDynamicSharedMemorySize, mlasp::kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(mlasp::mla_sparse_fwd_kernel<kInt8>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, mlasp::kSmemBytes);
+    if (e == cudaSuccess) {
+      // The warpgroups re-divide the registers the block is launched with;
+      // refuse to launch if the compiled per-thread count cannot cover them.
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, mlasp::mla_sparse_fwd_kernel<kInt8>);
+      using R = mlasp::Regs<kInt8>;
+      const long need = 256L * R::kSoftmax + 128L * 80 + 256L * R::kGather + 128L * R::kControl;
+      if (e == cudaSuccess && (fa.numRegs < 80 || static_cast<long>(fa.numRegs) * mlasp::kThreads < need))
+        e = cudaErrorInvalidConfiguration;
+    }
+    g_attr_err[dev][kInt8 ? 1 : 0] = e;
   });
   return g_attr_err[dev][kInt8 ? 1 : 0];
 }
@@ -646,7 +745,7 @@ mla_status mla_sparse_attn_fwd(const mla_dims* dims, const void* q_nope, const v
   if (dev < 0 || dev >= kMaxDevices) return fail(MLA_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
   const bool int8 = d.kv_dtype == MLA_KV_INT8;
   e = int8 ? prepare_kernel<true>(dev) : prepare_kernel<false>(dev);
-  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "kernel set-up: %s", cudaGetErrorString(e));
 
   mlasp::Params p;
   p.q_nope = static_cast<const uint16_t*>(q_nope);

@@ -9,9 +9,11 @@
 // Scores need all 576 dims: each CTA computes a partial score tile over its
 // 288 dims and sends it (fp32) to the peer through distributed shared memory;
 // both CTAs then hold bit-identical score tiles (fp32 addition commutes) and
-// run the same online softmax.  Sending is done by dedicated warps so that
-// the softmax warps never wait for remote stores to drain, and the softmax
-// runs one tile behind the score MMA so the exchange overlaps with it.
+// run the same online softmax.  Dedicated warps stage the partial tile in
+// local shared memory and hand it to the TMA engine as bulk copies into the
+// peer, so the CTA-to-CTA traffic never queues in front of other warps'
+// shared-memory accesses.  Each side reads its partial score tile out of
+// TMEM at once, so the next score MMA overlaps with the exchange.
 //
 // Per CTA (24 warps; registers rebalanced per warpgroup with setmaxnreg):
 //   warps 0-7   softmax: TMEM lane h = head h; warps w and w+4 share the
@@ -21,13 +23,14 @@
 //               and scale, row max across the warp pair, lazy online softmax,
 //               write P into TMEM as P_hi = bf16(p), P_lo = bf16(p - P_hi);
 //               final O / l -> bf16 and lse.
-//   warps 8-11  senders: read the partial S tile and push it to the peer.
-//   warps 12-19 gather: two groups of four warps, alternating key tiles; bf16
+//   warps 8-11  senders: partial S tile -> staging buffer -> bulk copy to the peer.
+//   warps 12-19 gather: all eight warps on every key tile (8 keys each); bf16
 //               cache by cp.async with zero fill for masked entries, INT8
 //               cache by loads, dequantisation to bf16 and stores.
-//   warp 20     MMA issue (one thread): S = Q K^T (A = Q latent in TMEM, rope
-//               in smem), O += P_hi V + P_lo V (A = P in TMEM, B = V MN-major).
-//   warp 21     index resolution: topk entry -> validity -> block_table -> row.
+//   warp 20     MMA issue (one thread, polling both hand-offs): S = Q K^T
+//               (A = Q latent in TMEM, rope in smem) and O += P_hi V + P_lo V
+//               (A = P in TMEM, B = V MN-major), each as soon as it is ready.
+//   warps 21-22 index resolution: topk entry -> validity -> block_table -> row.
 //
 // The stages follow "DeepSeek V3/V2 Sparse Flash Attention with Quantization",
 // section "Compute pipeline" (Sa_V0 gather + INT8 dequant, Sa_C1 S = Q K^T,
@@ -63,7 +66,9 @@ constexpr int kSenderWarp0 = 8;
 constexpr int kSenderThreads = 128;
 constexpr int kGatherWarp0 = 12;
 constexpr int kMmaWarp = 20;
-constexpr int kIndexWarp = 21;
+constexpr int kIndexWarp = 21;   // warps 21 and 22
+constexpr int kIndexWarps = 2;
+constexpr int kIdxBatch = 4;     // tiles resolved per index-warp pass
 // register shares (launch: 768 threads x 80 registers = 61,440)
 template <bool kInt8>
 struct Regs {
@@ -74,17 +79,27 @@ struct Regs {
 };
 
 constexpr int kTileKeys = 64;
-constexpr int kStages = 4;
-constexpr int kIdxSlots = 4;
+#ifndef MLA_STAGES
+#define MLA_STAGES 4
+#endif
+#ifndef MLA_RECV_SLOTS
+#define MLA_RECV_SLOTS 1
+#endif
+constexpr int kStages = MLA_STAGES;
+constexpr int kRecvSlots = MLA_RECV_SLOTS;
+constexpr int kIdxSlots = kIndexWarps * kIdxBatch;
 constexpr int kHeads = 128;
 constexpr int kChunkBytes = kTileKeys * 128;            // 64 keys x 64 bf16 latent dims (128-byte swizzle)
 constexpr int kRopeChunkBytes = kTileKeys * 64;         // 64 keys x 32 bf16 rope dims (64-byte swizzle)
 constexpr int kStageBytes = 4 * kChunkBytes + kRopeChunkBytes;
 constexpr int kRecvSlotBytes = kHeads * kTileKeys * 4;  // fp32 partial score tile
+constexpr int kXchgHalfBytes = kRecvSlotBytes / 2;       // key columns [32c, 32c + 32) of all heads
+constexpr int kXchgBlockBytes = 32 * 32 * 4;            // 32 heads x 32 keys: one bulk copy
 constexpr int kQRopeBytes = kHeads * 64;
 
 constexpr int kOffRecv = 0;                             // same offset in both CTAs (peer writes here)
-constexpr int kOffStages = kOffRecv + 2 * kRecvSlotBytes;
+constexpr int kOffStaging = kOffRecv + kRecvSlots * kRecvSlotBytes;
+constexpr int kOffStages = kOffStaging + kRecvSlotBytes;
 constexpr int kOffQRope = kOffStages + kStages * kStageBytes;
 constexpr int kOffRows = kOffQRope + kQRopeBytes;       // int32 [kIdxSlots][64]
 constexpr int kOffPair = kOffRows + kIdxSlots * kTileKeys * 4;
@@ -94,30 +109,34 @@ constexpr int kBarFull = 0;
 constexpr int kBarEmpty = kBarFull + kStages;
 constexpr int kBarIdxFull = kBarEmpty + kStages;
 constexpr int kBarIdxEmpty = kBarIdxFull + kIdxSlots;
-constexpr int kBarSFull = kBarIdxEmpty + kIdxSlots;
-constexpr int kBarSFree = kBarSFull + 1;
-constexpr int kBarPFull = kBarSFree + 1;
-constexpr int kBarPvDone = kBarPFull + 1;
-constexpr int kBarRecvFull = kBarPvDone + 1;   // [2]
-constexpr int kBarPeerFree = kBarRecvFull + 2;  // [2]
-constexpr int kBarPairA = kBarPeerFree + 2;     // [4]
+// S/P ping-pong: tile i uses TMEM region i % 2 and barrier [i % 2] of each pair
+constexpr int kBarSFull = kBarIdxEmpty + kIdxSlots;      // [2] S(i) computed
+constexpr int kBarSFree = kBarSFull + 2;                 // [2] senders have read S(i)
+constexpr int kBarPFull = kBarSFree + 2;                 // [2] P(i) written
+constexpr int kBarPvDone = kBarPFull + 2;                // [2] P(i).V accumulated
+constexpr int kBarRecvFull = kBarPvDone + 2;             // [kRecvSlots]
+constexpr int kBarPeerFree = kBarRecvFull + kRecvSlots;  // [kRecvSlots]
+constexpr int kBarPairA = kBarPeerFree + kRecvSlots;     // [4]
 constexpr int kBarPairB = kBarPairA + 4;        // [4]
 constexpr int kBarQReady = kBarPairB + 4;
 constexpr int kBarFinal = kBarQReady + 1;
 constexpr int kNumBars = kBarFinal + 1;
 constexpr int kOffTmemSlot = kOffBars + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
-constexpr int kSmemBytes = kOffAbort + 4;
+constexpr int kOffZero = kOffAbort + 4;  // a zero the compiler cannot see (dependency anchor)
+constexpr int kSmemBytes = kOffZero + 4;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffStages % 1024 == 0 && kStageBytes % 1024 == 0 && kOffQRope % 512 == 0, "operand alignment");
+static_assert(kOffStaging % 16 == 0 && kRecvSlotBytes % 16 == 0, "bulk copy alignment");
 static_assert(kOffBars % 8 == 0, "barrier alignment");
 
-// TMEM columns (512 allocated): O | S | P_hi | P_lo | Q latent half (bf16 pairs)
+// TMEM columns (512 allocated): O | region 0 | region 1 | Q latent half (bf16
+// pairs).  Tile i's score tile S(i) (64 fp32 columns) lands in region i % 2;
+// once it has been read out, P(i) overwrites it as P_hi (columns 0-31 of the
+// region) and P_lo (columns 32-63), each 64 bf16 keys per row.
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;
-constexpr uint32_t kTmemS = 256;
-constexpr uint32_t kTmemPhi = 320;
-constexpr uint32_t kTmemPlo = 352;
+constexpr uint32_t kTmemRegion = 256;  // + 64 * (i % 2)
 constexpr uint32_t kTmemQ = 384;
 
 constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;
@@ -172,47 +191,59 @@ __device__ __forceinline__ float4 lds16f(uint32_t addr) {
                : "memory");
   return v;
 }
-// 16-byte unit u (0..15) of score row h in a receive slot, XOR-swizzled so a
-// warp's 32 rows spread over all banks.
-__device__ __forceinline__ uint32_t recv_unit(int h, int u) {
-  return static_cast<uint32_t>(h * 256 + ((u ^ (h & 15)) << 4));
+// Exchange layout of a partial score tile (staging buffer and receive slots):
+// column half c (keys [32c, 32c + 32)) of all heads is one 16 KB block, head h
+// a 128-byte row in it, 16-byte unit k (keys 32c + 4k .. 32c + 4k + 3) of row h
+// at k ^ (h & 7), so a warp's 32 rows spread over all banks.  The 32 rows of a
+// TMEM lane quadrant form one contiguous 4 KB block per column half.
+__device__ __forceinline__ uint32_t xchg_offset(int h, int c, int k) {
+  return static_cast<uint32_t>(c * kXchgHalfBytes + h * 128 + ((k ^ (h & 7)) << 4));
 }
 
 // ------------------------------------------------------------------ index warp
-__device__ void index_role(const Params& p, const Ctx& c, int lane) {
+// Two index warps take alternate passes of kIdxBatch tiles (warp iw owns the
+// ring slots [kIdxBatch iw, kIdxBatch iw + kIdxBatch)), so two chains of
+// dependent loads (top-k entry, then block_table) are in flight at once.
+__device__ void index_role(const Params& p, const Ctx& c, int iw, int lane) {
   const int b = c.t / p.S1;
   const int act = __ldg(p.act_seqs + b);
   const int32_t* tk = p.topk_idx + static_cast<int64_t>(c.t) * p.topk;
   const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.mbps;
   int32_t* rows = reinterpret_cast<int32_t*>(c.smem + kOffRows);
+  // pull this token's top-k row and its sequence's block-table row towards
+  // L2 up front (one 128-byte line per prefetch; the warps split the lines)
+  for (int e = (iw * 32 + lane) * 32; e < p.topk + 32; e += kIndexWarps * 32 * 32) prefetch_l2(tk + min(e, p.topk - 1));
+  for (int e = (iw * 32 + lane) * 32; e < p.mbps + 32; e += kIndexWarps * 32 * 32) prefetch_l2(bt + min(e, p.mbps - 1));
   bool bad = false;
-  for (int j0 = 0; j0 < p.n_tiles; j0 += 2) {
-    const int nb = min(2, p.n_tiles - j0);
+  for (int j0 = iw * kIdxBatch; j0 < p.n_tiles; j0 += kIndexWarps * kIdxBatch) {
+    const int nb = min(kIdxBatch, p.n_tiles - j0);
     bool ok = true;
     for (int k = 0; k < nb && ok; ++k) {
       const int j = j0 + k;
       ok = warp_wait(c, kBarIdxEmpty + (j % kIdxSlots), ((j / kIdxSlots) & 1) ^ 1);
     }
     if (!ok) break;
-    int idx[4], blk[4];
+    static_assert(kIdxBatch == 4, "two entries per lane per tile, four tiles per pass");
+    int idx[8], blk[8];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < 8; ++q) {
       const int e = (j0 + (q >> 1)) * kTileKeys + (q & 1) * 32 + lane;
       idx[q] = ((q >> 1) < nb && e < p.topk) ? __ldg(tk + e) : -1;
     }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < 8; ++q) {
       const bool valid = idx[q] >= 0 && idx[q] < act;
       const int slot = idx[q] >> 7;
       blk[q] = (valid && slot < p.mbps) ? __ldg(bt + slot) : -1;
       if (valid && (blk[q] < 0 || blk[q] >= p.num_blocks)) bad = true;
     }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < 8; ++q) {
       if ((q >> 1) >= nb) continue;
       const bool valid = idx[q] >= 0 && idx[q] < act && blk[q] >= 0 && blk[q] < p.num_blocks;
       const int j = j0 + (q >> 1);
-      rows[(j % kIdxSlots) * kTileKeys + (q & 1) * 32 + lane] = valid ? (blk[q] * 128 + (idx[q] & 127)) : -1;
+      const int row = blk[q] * 128 + (idx[q] & 127);
+      rows[(j % kIdxSlots) * kTileKeys + (q & 1) * 32 + lane] = valid ? row : -1;
     }
     for (int k = 0; k < nb; ++k) mbar_arrive(c.bar(kBarIdxFull + ((j0 + k) % kIdxSlots)));
   }
@@ -241,43 +272,40 @@ __device__ __forceinline__ void dequant4(uint32_t w, float s, uint32_t& lo, uint
 
 template <bool kInt8>
 __device__ void gather_role(const Params& p, const Ctx& c, int gw, int lane) {
-  const int g = gw >> 2;  // tiles j with j % 2 == g
-  const int w4 = gw & 3;  // keys [16 w4, 16 w4 + 16)
-  const int key0 = w4 * 16;
+  // all eight warps work on every tile; warp gw takes keys [8 gw, 8 gw + 8)
+  const int key0 = gw * 8;
   const int32_t* rows_all = reinterpret_cast<const int32_t*>(c.smem + kOffRows);
-  uint16_t* vmask16 = reinterpret_cast<uint16_t*>(c.smem + kOffVmask);
+  uint8_t* vmask8 = c.smem + kOffVmask;
   const uint8_t* kvr = reinterpret_cast<const uint8_t*>(p.kv_rope) + c.crank * 64 + (lane & 3) * 16;
-  const int rk0 = key0 + (lane >> 2), rk1 = key0 + 8 + (lane >> 2);
-  for (int j = g; j < p.n_tiles; j += 2) {
+  const int rk = key0 + (lane >> 2);  // rope: four 16-byte units per key, one per lane
+  for (int j = 0; j < p.n_tiles; ++j) {
     const int st = j % kStages;
     const int slot = j % kIdxSlots;
     if (!warp_wait(c, kBarEmpty + st, ((j / kStages) & 1) ^ 1)) break;
     if (!warp_wait(c, kBarIdxFull + slot, (j / kIdxSlots) & 1)) break;
     const int32_t* rows = rows_all + slot * kTileKeys;
-    const uint32_t vbits = __ballot_sync(0xffffffffu, lane < 16 && rows[key0 + (lane & 15)] >= 0) & 0xFFFFu;
-    const int32_t r0 = rows[rk0], r1 = rows[rk1];
+    const uint32_t vbits = __ballot_sync(0xffffffffu, lane < 8 && rows[key0 + (lane & 7)] >= 0) & 0xFFu;
+    const int32_t rr = rows[rk];
     const uint32_t stage = c.sbase + kOffStages + st * kStageBytes;
     const uint32_t rope = stage + 4 * kChunkBytes;
     if constexpr (!kInt8) {
       // latent half: 512 B per key, one key per warp instruction (32 lanes x 16 B)
       const uint8_t* kvn = reinterpret_cast<const uint8_t*>(p.kv_nope) + c.crank * 512 + lane * 16;
       const uint32_t chunk = stage + (lane >> 3) * kChunkBytes;
-#pragma unroll 4
-      for (int i = 0; i < 16; ++i) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
         const int key = key0 + i;
         const int32_t row = rows[key];
         cp_async_16(chunk + key * 128 + (((lane & 7) ^ (key & 7)) << 4),
                     row >= 0 ? kvn + static_cast<int64_t>(row) * 1024 : kvn, row >= 0 ? 16u : 0u);
       }
-      cp_async_16(rope + rope_unit(rk0, lane & 3), r0 >= 0 ? kvr + static_cast<int64_t>(r0) * 128 : kvr,
-                  r0 >= 0 ? 16u : 0u);
-      cp_async_16(rope + rope_unit(rk1, lane & 3), r1 >= 0 ? kvr + static_cast<int64_t>(r1) * 128 : kvr,
-                  r1 >= 0 ? 16u : 0u);
+      cp_async_16(rope + rope_unit(rk, lane & 3), rr >= 0 ? kvr + static_cast<int64_t>(rr) * 128 : kvr,
+                  rr >= 0 ? 16u : 0u);
       mbar_arrive_relaxed(c.bar(kBarIdxEmpty + slot));
       cp_async_arrive_noinc(c.bar(kBarFull + st));
       if (lane == 0) {
-        vmask16[st * 4 + w4] = static_cast<uint16_t>(vbits);
-        mbar_arrive(c.bar(kBarFull + st));  // releases the mask word
+        vmask8[st * 8 + gw] = static_cast<uint8_t>(vbits);
+        mbar_arrive(c.bar(kBarFull + st));  // releases the mask byte
       }
     } else {
       const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
@@ -285,21 +313,20 @@ __device__ void gather_role(const Params& p, const Ctx& c, int gw, int lane) {
       const int u = lane & 15;
       const int8_t* kvn = reinterpret_cast<const int8_t*>(p.kv_nope) + c.crank * 256 + u * 16;
       const float* scl = p.kv_scales + c.crank * 2 + (u >> 3);
-      uint4 v[8];
-      float sc[8];
+      uint4 v[4];
+      float sc[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < 4; ++i) {
         const int32_t row = rows[key0 + 2 * i + (lane >> 4)];
         v[i] = row >= 0 ? ldg16(kvn + static_cast<int64_t>(row) * 512) : zero;
         sc[i] = row >= 0 ? __ldg(scl + static_cast<int64_t>(row) * 4) : 0.f;
       }
-      const uint4 q0 = r0 >= 0 ? ldg16(kvr + static_cast<int64_t>(r0) * 128) : zero;
-      const uint4 q1 = r1 >= 0 ? ldg16(kvr + static_cast<int64_t>(r1) * 128) : zero;
+      const uint4 qr = rr >= 0 ? ldg16(kvr + static_cast<int64_t>(rr) * 128) : zero;
       mbar_arrive_relaxed(c.bar(kBarIdxEmpty + slot));
       const uint32_t chunk = stage + (u >> 2) * kChunkBytes;
       const int u8 = (u & 3) * 2;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < 4; ++i) {
         const int key = key0 + 2 * i + (lane >> 4);
         uint4 a, b2;
         dequant4(v[i].x, sc[i], a.x, a.y);
@@ -309,9 +336,8 @@ __device__ void gather_role(const Params& p, const Ctx& c, int gw, int lane) {
         sts16(chunk + key * 128 + ((u8 ^ (key & 7)) << 4), a);
         sts16(chunk + key * 128 + (((u8 + 1) ^ (key & 7)) << 4), b2);
       }
-      sts16(rope + rope_unit(rk0, lane & 3), q0);
-      sts16(rope + rope_unit(rk1, lane & 3), q1);
-      if (lane == 0) vmask16[st * 4 + w4] = static_cast<uint16_t>(vbits);
+      sts16(rope + rope_unit(rk, lane & 3), qr);
+      if (lane == 0) vmask8[st * 8 + gw] = static_cast<uint8_t>(vbits);
       fence_proxy_async_smem();
       mbar_arrive(c.bar(kBarFull + st));
     }
@@ -319,81 +345,121 @@ __device__ void gather_role(const Params& p, const Ctx& c, int gw, int lane) {
 }
 
 // ------------------------------------------------------------------ sender warps
-// Push the CTA's partial score tile (128 heads x 64 keys, fp32) to the peer.
+// Copy the CTA's partial score tile (128 heads x 64 keys, fp32) into the
+// peer's receive slot: TMEM -> registers -> the local staging buffer, then
+// bulk copies by the TMA engine, so the CTA-to-CTA traffic never queues in
+// front of the softmax warps' shared-memory accesses.
 __device__ void sender_role(const Params& p, const Ctx& c, int q, int lane) {
   const int h = q * 32 + lane;
-  const uint32_t tS = c.tmem + (static_cast<uint32_t>(q * 32) << 16) + kTmemS;
+  const uint32_t tS = c.tmem + (static_cast<uint32_t>(q * 32) << 16) + kTmemRegion;
   const uint32_t peer = c.crank ^ 1u;
+  const uint32_t stg = c.sbase + kOffStaging;
   const uint32_t recv_remote = mapa_shared(c.sbase + kOffRecv, peer);
   for (int j = 0; j < p.n_tiles; ++j) {
-    if (!warp_wait(c, kBarSFull, j & 1)) break;
+    if (!warp_wait(c, kBarSFull + (j & 1), (j >> 1) & 1)) break;
     tc_fence_after();
-    uint32_t r[64];
-    {
-      uint32_t a[32], b[32];
-      tmem_ld_32x32b_x32(tS, a);
-      tmem_ld_32x32b_x32(tS + 32, b);
-      tmem_wait_ld();
+    uint32_t a[32], b[32];
+    tmem_ld_32x32b_x32(tS + 64 * (j & 1), a);
+    tmem_ld_32x32b_x32(tS + 64 * (j & 1) + 32, b);
+    tmem_wait_ld();
+    tc_fence_before();
+    mbar_arrive_relaxed(c.bar(kBarSFree + (j & 1)));  // the values are in registers (wait::ld)
+    if (lane == 0) bulk_wait_read_all();    // the previous tile has left the staging buffer
+    __syncwarp();
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        r[i] = a[i];
-        r[32 + i] = b[i];
+    for (int k = 0; k < 8; ++k) {
+      sts16(stg + xchg_offset(h, 0, k), make_uint4(a[4 * k], a[4 * k + 1], a[4 * k + 2], a[4 * k + 3]));
+      sts16(stg + xchg_offset(h, 1, k), make_uint4(b[4 * k], b[4 * k + 1], b[4 * k + 2], b[4 * k + 3]));
+    }
+    fence_proxy_async_smem();  // generic-proxy stores -> bulk-copy reads
+    __syncwarp();
+    const int slot = j % kRecvSlots, use = j / kRecvSlots;
+    bool ok = true;
+    if (lane == 0) {
+      if (use > 0) ok = mbar_wait<true>(c.bar(kBarPeerFree + slot), (use & 1) ^ 1, c.abort, kWaitLimitNs);
+      if (ok) {
+        const uint32_t rbar = mapa_shared(c.bar(kBarRecvFull + slot), peer);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const uint32_t off = xchg_offset(q * 32, half, 0);
+          bulk_copy_to_peer(recv_remote + slot * kRecvSlotBytes + off, stg + off, kXchgBlockBytes, rbar);
+        }
+        bulk_commit();
       }
     }
-    tc_fence_before();
-    mbar_arrive_relaxed(c.bar(kBarSFree));  // the values are in registers (wait::ld)
-    const int b = j & 1;
-    if (j >= 2 && !warp_wait_cluster(c, kBarPeerFree + b, ((j >> 1) & 1) ^ 1)) break;
-    const uint32_t dst = recv_remote + b * kRecvSlotBytes;
-    const uint32_t rbar = mapa_shared(c.bar(kBarRecvFull + b), peer);
-#pragma unroll
-    for (int u = 0; u < 16; ++u)
-      st_async_v4(dst + recv_unit(h, u), r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3], rbar);
+    if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
   }
+  // the peer cannot leave before this CTA reaches its final cluster barrier,
+  // which waits for these copies to complete
+  if (lane == 0) bulk_wait_all();
+  __syncwarp();
 }
 
 // ------------------------------------------------------------------ MMA warp
-__device__ __forceinline__ bool issue_pv(const Ctx& c, int i) {
-  if (!wait_bar(c, kBarPFull, i & 1)) return false;
+__device__ __forceinline__ void issue_s(const Ctx& c, int k) {
+  constexpr uint32_t idesc = make_idesc_f16(128, 64, 1, 0, 0);
+  const uint32_t qrope = c.sbase + kOffQRope;
+  const uint32_t stage = c.sbase + kOffStages + (k % kStages) * kStageBytes;
+  fence_proxy_async_smem();  // cp.async / st.shared data -> tensor-core reads
   tc_fence_after();
+  // S = Q_latent K_latent^T (A = Q in TMEM) + Q_rope K_rope^T (A = Q rope in smem)
+#pragma unroll
+  const uint32_t dS = c.tmem + kTmemRegion + 64 * (k & 1);
+  for (int s = 0; s < 16; ++s)
+    umma_ts(dS, c.tmem + kTmemQ + 8 * s,
+            make_sdesc(stage + (s >> 2) * kChunkBytes + (s & 3) * 32, 16, 1024, kSwizzle128B), idesc, s > 0 ? 1u : 0u);
+#pragma unroll
+  for (int s = 0; s < 2; ++s)
+    umma_ss(dS, make_sdesc(qrope + s * 32, 16, 512, kSwizzle64B),
+            make_sdesc(stage + 4 * kChunkBytes + s * 32, 16, 512, kSwizzle64B), idesc, 1u);
+  umma_commit(c.bar(kBarSFull + (k & 1)));
+}
+
+__device__ __forceinline__ void issue_pv(const Ctx& c, int i) {
   constexpr uint32_t idesc = make_idesc_f16(128, 256, 1, 0, 1);
   const uint32_t stage = c.sbase + kOffStages + (i % kStages) * kStageBytes;
+  const uint32_t aP = c.tmem + kTmemRegion + 64 * (i & 1);
+  tc_fence_after();
   // O += P_hi . V, then O += P_lo . V (same V tile, 16 keys per instruction)
 #pragma unroll
   for (int s = 0; s < 8; ++s)
-    umma_ts(c.tmem + kTmemO, c.tmem + (s < 4 ? kTmemPhi : kTmemPlo) + 8 * (s & 3),
+    umma_ts(c.tmem + kTmemO, aP + (s < 4 ? 0 : 32) + 8 * (s & 3),
             make_sdesc(stage + (s & 3) * 16 * 128, kChunkBytes, 1024, kSwizzle128B), idesc,
             (i > 0 || s > 0) ? 1u : 0u);
-  umma_commit(c.bar(kBarPvDone));
+  umma_commit(c.bar(kBarPvDone + (i & 1)));
   umma_commit(c.bar(kBarEmpty + (i % kStages)));
-  return true;
 }
 
+// One thread polls both hand-offs and issues whichever is ready: P.V(kp) as
+// soon as the softmax has written P(kp), and S(ks) once its key tile has
+// landed and P.V(ks - 2) has released TMEM region ks % 2, so a stage is
+// released as early as the data allows and the softmax of one tile overlaps
+// with the P.V of the previous one.
 __device__ void mma_role(const Params& p, const Ctx& c) {
-  constexpr uint32_t idesc_s = make_idesc_f16(128, 64, 1, 0, 0);
-  const uint32_t qrope = c.sbase + kOffQRope;
   bool ok = wait_bar(c, kBarQReady, 0);
-  // Issue order S(k), P.V(k-2): the softmax runs one tile behind the score MMA.
-  for (int k = 0; ok && k < p.n_tiles + 2; ++k) {
-    if (k < p.n_tiles) {
-      const int st = k % kStages;
-      if (!wait_bar(c, kBarFull + st, (k / kStages) & 1)) { ok = false; break; }
-      if (k > 0 && !wait_bar(c, kBarSFree, (k - 1) & 1)) { ok = false; break; }
-      fence_proxy_async_smem();  // cp.async / st.shared data -> tensor-core reads
-      tc_fence_after();
-      const uint32_t stage = c.sbase + kOffStages + st * kStageBytes;
-#pragma unroll
-      for (int s = 0; s < 16; ++s)
-        umma_ts(c.tmem + kTmemS, c.tmem + kTmemQ + 8 * s,
-                make_sdesc(stage + (s >> 2) * kChunkBytes + (s & 3) * 32, 16, 1024, kSwizzle128B), idesc_s,
-                s > 0 ? 1u : 0u);
-#pragma unroll
-      for (int s = 0; s < 2; ++s)
-        umma_ss(c.tmem + kTmemS, make_sdesc(qrope + s * 32, 16, 512, kSwizzle64B),
-                make_sdesc(stage + 4 * kChunkBytes + s * 32, 16, 512, kSwizzle64B), idesc_s, 1u);
-      umma_commit(c.bar(kBarSFull));
+  int ks = 0, kp = 0;
+  uint64_t t_idle = 0;
+  uint32_t spins = 0;
+  while (ok && kp < p.n_tiles) {
+    bool progressed = false;
+    if (kp < ks && mbar_poll(c.bar(kBarPFull + (kp & 1)), (kp >> 1) & 1)) {
+      issue_pv(c, kp++);
+      progressed = true;
     }
-    if (k >= 2 && !issue_pv(c, k - 2)) { ok = false; break; }
+    if (ks < p.n_tiles && mbar_poll(c.bar(kBarFull + ks % kStages), (ks / kStages) & 1) &&
+        (ks < 2 || mbar_poll(c.bar(kBarPvDone + (ks & 1)), ((ks >> 1) & 1) ^ 1))) {
+      issue_s(c, ks++);
+      progressed = true;
+    }
+    if (progressed) {
+      spins = 0;
+    } else if ((++spins & 255u) == 0) {
+      // bounded like every other wait: give up after the limit without progress
+      const uint64_t now = globaltimer_ns();
+      if (t_idle == 0 || spins == 256u) t_idle = now;
+      if (*c.abort) ok = false;
+      else if (now - t_idle > kWaitLimitNs) { *c.abort = 1u; ok = false; }
+    }
   }
   umma_commit(c.bar(kBarFinal));
   volatile uint32_t never = 0;
@@ -407,9 +473,7 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
   const int h = q * 32 + lane;     // head
   const int tid = warp * 32 + lane;
   const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-  const uint32_t tS = c.tmem + lane_off + kTmemS + 32 * half;
-  const uint32_t tPhi = c.tmem + lane_off + kTmemPhi + 16 * half;
-  const uint32_t tPlo = c.tmem + lane_off + kTmemPlo + 16 * half;
+  const uint32_t tR = c.tmem + lane_off + kTmemRegion;  // + 64 * (i % 2)
   const uint32_t tO = c.tmem + lane_off + kTmemO + 128 * half;
   const uint32_t tQ = c.tmem + lane_off + kTmemQ + 64 * half;
   const bool live = h < p.n_q;
@@ -444,42 +508,42 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
     mbar_arrive(c.bar(kBarQReady));
   }
   const uint32_t peer = c.crank ^ 1u;
+  const uint32_t dep_zero = *reinterpret_cast<volatile uint32_t*>(c.smem + kOffZero);
   float* pair = reinterpret_cast<float*>(c.smem + kOffPair);
   const uint64_t* vmask = reinterpret_cast<const uint64_t*>(c.smem + kOffVmask);
   const float scl = p.scale_log2;
   float m = -INFINITY, l = 0.f;
-  float own_prev[32];
   bool ok = true;
-  for (int j = 0; j <= p.n_tiles; ++j) {
-    float own_cur[32];
-    if (j < p.n_tiles) {
-      // own partial score tile j (kept until the peer's partial arrives)
-      if (!warp_wait(c, kBarSFull, j & 1)) { ok = false; break; }
+  for (int i = 0; i < p.n_tiles; ++i) {
+    {
+      // own partial score tile i, read out at once so the next score MMA can
+      // start while the peer's partial is still on its way
+      const uint32_t reg = tR + 64 * (i & 1);
+      if (!warp_wait(c, kBarSFull + (i & 1), (i >> 1) & 1)) { ok = false; break; }
       tc_fence_after();
-      uint32_t r[32];
-      tmem_ld_32x32b_x32(tS, r);
+      uint32_t own[32];
+      tmem_ld_32x32b_x32(reg + 32 * half, own);
       tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive_relaxed(c.bar(kBarSFree));
-#pragma unroll
-      for (int i = 0; i < 32; ++i) own_cur[i] = __uint_as_float(r[i]);
-    }
-    if (j >= 1) {
-      const int i = j - 1;  // tile whose softmax runs now
-      const int b = i & 1;
-      if (!warp_wait_cluster(c, kBarRecvFull + b, (i >> 1) & 1)) { ok = false; break; }
-      if (tid == 0 && i + 2 < p.n_tiles) mbar_arrive_expect_tx(c.bar(kBarRecvFull + b), kRecvSlotBytes);
+      tc_fence_before();  // ordered before the row-max handshake that precedes P(i) stores
+      const int b = i % kRecvSlots;
+      if (!warp_wait_cluster(c, kBarRecvFull + b, (i / kRecvSlots) & 1)) { ok = false; break; }
+      if (tid == 0 && i + kRecvSlots < p.n_tiles) mbar_arrive_expect_tx(c.bar(kBarRecvFull + b), kRecvSlotBytes);
       float s[32];
       const uint32_t slot = c.sbase + kOffRecv + b * kRecvSlotBytes;
+      uint32_t dep = 0;
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const float4 v = lds16f(slot + recv_unit(h, 8 * half + k));
-        s[4 * k + 0] = own_prev[4 * k + 0] + v.x;
-        s[4 * k + 1] = own_prev[4 * k + 1] + v.y;
-        s[4 * k + 2] = own_prev[4 * k + 2] + v.z;
-        s[4 * k + 3] = own_prev[4 * k + 3] + v.w;
+        const float4 v = lds16f(slot + xchg_offset(h, half, k));
+        s[4 * k + 0] = __uint_as_float(own[4 * k + 0]) + v.x;
+        s[4 * k + 1] = __uint_as_float(own[4 * k + 1]) + v.y;
+        s[4 * k + 2] = __uint_as_float(own[4 * k + 2]) + v.z;
+        s[4 * k + 3] = __uint_as_float(own[4 * k + 3]) + v.w;
+        dep ^= __float_as_uint(v.x) ^ __float_as_uint(v.w);
       }
-      mbar_arrive_remote_relaxed(mapa_shared(c.bar(kBarPeerFree + b), peer));  // the values were consumed
+      // Free the slot for the peer.  The arrive's address depends on every
+      // loaded value (dep & dep_zero, a run-time 0), so it cannot issue
+      // before the loads have returned and needs no release fence.
+      mbar_arrive_remote_relaxed(mapa_shared(c.bar(kBarPeerFree + b), peer) + (dep & dep_zero));
       // mask (waiting on the stage barrier acquires the gather's validity bits) and scale
       if (!warp_wait(c, kBarFull + (i % kStages), (i / kStages) & 1)) { ok = false; break; }
       const uint32_t vm = static_cast<uint32_t>(vmask[i % kStages] >> (32 * half));
@@ -506,7 +570,8 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
         m = mx;
       }
       if (__any_sync(0xffffffffu, grow) && i > 0) {
-        if (!warp_wait(c, kBarPvDone, (i - 1) & 1)) { ok = false; break; }
+        // O may only be rescaled once P(i-1).V has been accumulated into it
+        if (!warp_wait(c, kBarPvDone + ((i - 1) & 1), ((i - 1) >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {
@@ -533,18 +598,17 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
         plo[k] = pack_bf16x2(p0 - __uint_as_float(hw << 16), p1 - __uint_as_float(hw & 0xFFFF0000u));
       }
       l += lsum;
-      if (i > 0) {
-        if (!warp_wait(c, kBarPvDone, (i - 1) & 1)) { ok = false; break; }
-        tc_fence_after();
-      }
-      tmem_st_32x32b_x16(tPhi, phi);
-      tmem_st_32x32b_x16(tPlo, plo);
+      // P(i) overwrites S(i) in its region: the senders must have read it out
+      // (this warp and its pair partner read their own columns before the
+      // row-max handshake above)
+      if (!warp_wait(c, kBarSFree + (i & 1), (i >> 1) & 1)) { ok = false; break; }
+      tc_fence_after();
+      tmem_st_32x32b_x16(reg + 16 * half, phi);
+      tmem_st_32x32b_x16(reg + 32 + 16 * half, plo);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(c.bar(kBarPFull));
+      mbar_arrive(c.bar(kBarPFull + (i & 1)));
     }
-#pragma unroll
-    for (int k = 0; k < 32; ++k) own_prev[k] = own_cur[k];
   }
   if (!ok) return;
   // l over the whole row: add the partner's column half (same order in both threads)
@@ -552,7 +616,7 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
   mbar_arrive(c.bar(kBarPairA + q));
   if (!warp_wait(c, kBarPairA + q, p.n_tiles & 1)) return;
   const float l_tot = half == 0 ? l + pair[kHeads + h] : pair[h] + l;
-  if (!warp_wait(c, kBarPvDone, (p.n_tiles - 1) & 1)) return;
+  if (!warp_wait(c, kBarPvDone + ((p.n_tiles - 1) & 1), ((p.n_tiles - 1) >> 1) & 1)) return;
   tc_fence_after();
   const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
   uint4* op = reinterpret_cast<uint4*>(p.out + qrow * 512 + c.crank * 256 + half * 128);
@@ -594,18 +658,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_spa
     *c.abort = ((*reinterpret_cast<volatile unsigned int*>(&g_mla_status) & MLA_DEVICE_TIMEOUT) || misaligned) ? 1u : 0u;
     if (misaligned) atomicOr(&g_mla_status, MLA_DEVICE_TIMEOUT);
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(c.bar(kBarFull + i), kInt8 ? 128 : 128 + 4);
+      mbar_init(c.bar(kBarFull + i), kInt8 ? 256 : 256 + 8);
       mbar_init(c.bar(kBarEmpty + i), 1);
     }
     for (int i = 0; i < kIdxSlots; ++i) {
       mbar_init(c.bar(kBarIdxFull + i), 32);
-      mbar_init(c.bar(kBarIdxEmpty + i), 128);
+      mbar_init(c.bar(kBarIdxEmpty + i), 256);
     }
-    mbar_init(c.bar(kBarSFull), 1);
-    mbar_init(c.bar(kBarSFree), kSoftmaxThreads + kSenderThreads);
-    mbar_init(c.bar(kBarPFull), kSoftmaxThreads);
-    mbar_init(c.bar(kBarPvDone), 1);
-    for (int b = 0; b < 2; ++b) {
+    for (int r = 0; r < 2; ++r) {
+      mbar_init(c.bar(kBarSFull + r), 1);
+      mbar_init(c.bar(kBarSFree + r), kSenderThreads);
+      mbar_init(c.bar(kBarPFull + r), kSoftmaxThreads);
+      mbar_init(c.bar(kBarPvDone + r), 1);
+    }
+    for (int b = 0; b < kRecvSlots; ++b) {
       mbar_init(c.bar(kBarRecvFull + b), 1);
       mbar_init(c.bar(kBarPeerFree + b), kSoftmaxThreads);
     }
@@ -616,7 +682,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_spa
     mbar_init(c.bar(kBarQReady), kSoftmaxThreads);
     mbar_init(c.bar(kBarFinal), 1);
     fence_mbarrier_init_cluster();
-    for (int b = 0; b < 2; ++b) mbar_arrive_expect_tx(c.bar(kBarRecvFull + b), kRecvSlotBytes);
+    for (int b = 0; b < kRecvSlots; ++b) mbar_arrive_expect_tx(c.bar(kBarRecvFull + b), kRecvSlotBytes);
+    *reinterpret_cast<volatile uint32_t*>(smem + kOffZero) = 0u;
   }
   if (warp == kMmaWarp) {
     tmem_alloc(c.sbase + kOffTmemSlot, kTmemCols);
@@ -642,8 +709,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_spa
       if (warp == kMmaWarp) {
         if (lane == 0) mma_role(p, c);
         __syncwarp();
-      } else if (warp == kIndexWarp) {
-        index_role(p, c, lane);
+      } else if (warp < kIndexWarp + kIndexWarps) {
+        index_role(p, c, warp - kIndexWarp, lane);
       }
     }
   }

@@ -18,12 +18,13 @@
 // Per CTA (24 warps; registers rebalanced per warpgroup with setmaxnreg):
 //   warps 0-7   softmax: TMEM lane h = head h; warps w and w+4 share the
 //               lanes of quadrant w % 4 and take key columns [32c, 32c+32),
-//               c = w / 4.  Load Q (latent half into TMEM, rope half into
-//               smem); per tile keep the own partial S, add the peer's, mask
-//               and scale, row max across the warp pair, lazy online softmax,
-//               write P into TMEM as P_hi = bf16(p), P_lo = bf16(p - P_hi);
-//               final O / l -> bf16 and lse.
-//   warps 8-11  senders: partial S tile -> staging buffer -> bulk copy to the peer.
+//               c = w / 4.  Load Q (latent dims [0, 128) into TMEM, [128, 256)
+//               and the rope dims into smem); per tile read the own partial S,
+//               add the peer's, mask and scale, row max across the warp pair,
+//               lazy online softmax, write P over S in its TMEM region as
+//               P_hi = bf16(p), P_lo = bf16(p - P_hi); final O / l -> bf16, lse.
+//   warps 8-11  senders: partial S tile -> staging buffer -> bulk copies to
+//               the peer, one 32-key column half at a time.
 //   warps 12-19 gather: all eight warps on every key tile (8 keys each); bf16
 //               cache by cp.async with zero fill for masked entries, INT8
 //               cache by loads, dequantisation to bf16 and stores.
@@ -74,33 +75,28 @@ template <bool kInt8>
 struct Regs {
   static constexpr uint32_t kSoftmax = kInt8 ? 120 : 136;
   static constexpr uint32_t kGather = kInt8 ? 56 : 40;
-  static constexpr uint32_t kControl = 40;
+  static constexpr uint32_t kControl = 48;
   static_assert(256 * kSoftmax + 128 * 80 + 256 * kGather + 128 * kControl <= 768 * 80, "register budget");
 };
 
 constexpr int kTileKeys = 64;
-#ifndef MLA_STAGES
-#define MLA_STAGES 4
-#endif
-#ifndef MLA_RECV_SLOTS
-#define MLA_RECV_SLOTS 1
-#endif
-constexpr int kStages = MLA_STAGES;
-constexpr int kRecvSlots = MLA_RECV_SLOTS;
+constexpr int kStages = 4;
+constexpr int kRegions = 3;  // TMEM score/P regions: tiles i, i+1, i+2 in flight
 constexpr int kIdxSlots = kIndexWarps * kIdxBatch;
 constexpr int kHeads = 128;
 constexpr int kChunkBytes = kTileKeys * 128;            // 64 keys x 64 bf16 latent dims (128-byte swizzle)
 constexpr int kRopeChunkBytes = kTileKeys * 64;         // 64 keys x 32 bf16 rope dims (64-byte swizzle)
 constexpr int kStageBytes = 4 * kChunkBytes + kRopeChunkBytes;
-constexpr int kRecvSlotBytes = kHeads * kTileKeys * 4;  // fp32 partial score tile
-constexpr int kXchgHalfBytes = kRecvSlotBytes / 2;       // key columns [32c, 32c + 32) of all heads
-constexpr int kXchgBlockBytes = 32 * 32 * 4;            // 32 heads x 32 keys: one bulk copy
+constexpr int kXchgBytes = kHeads * 32 * 4;            // one column half (32 keys) of an fp32 partial score tile
+constexpr int kXchgBlockBytes = 32 * 32 * 4;           // its 32 heads of one TMEM lane quadrant: one bulk copy
+constexpr int kQHalfBytes = kHeads * 128 * 2;          // Q latent dims [128, 256) of this CTA (bf16)
 constexpr int kQRopeBytes = kHeads * 64;
 
-constexpr int kOffRecv = 0;                             // same offset in both CTAs (peer writes here)
-constexpr int kOffStaging = kOffRecv + kRecvSlots * kRecvSlotBytes;
-constexpr int kOffStages = kOffStaging + kRecvSlotBytes;
-constexpr int kOffQRope = kOffStages + kStages * kStageBytes;
+constexpr int kOffRecv = 0;                            // same offset in both CTAs (peer writes here)
+constexpr int kOffStaging = kOffRecv + kXchgBytes;
+constexpr int kOffStages = kOffStaging + kXchgBytes;
+constexpr int kOffQHalf = kOffStages + kStages * kStageBytes;
+constexpr int kOffQRope = kOffQHalf + kQHalfBytes;
 constexpr int kOffRows = kOffQRope + kQRopeBytes;       // int32 [kIdxSlots][64]
 constexpr int kOffPair = kOffRows + kIdxSlots * kTileKeys * 4;
 constexpr int kOffVmask = kOffPair + 2 * kHeads * 4;    // uint64 [kStages]
@@ -109,14 +105,19 @@ constexpr int kBarFull = 0;
 constexpr int kBarEmpty = kBarFull + kStages;
 constexpr int kBarIdxFull = kBarEmpty + kStages;
 constexpr int kBarIdxEmpty = kBarIdxFull + kIdxSlots;
-// S/P ping-pong: tile i uses TMEM region i % 2 and barrier [i % 2] of each pair
-constexpr int kBarSFull = kBarIdxEmpty + kIdxSlots;      // [2] S(i) computed
-constexpr int kBarSFree = kBarSFull + 2;                 // [2] senders have read S(i)
-constexpr int kBarPFull = kBarSFree + 2;                 // [2] P(i) written
-constexpr int kBarPvDone = kBarPFull + 2;                // [2] P(i).V accumulated
-constexpr int kBarRecvFull = kBarPvDone + 2;             // [kRecvSlots]
-constexpr int kBarPeerFree = kBarRecvFull + kRecvSlots;  // [kRecvSlots]
-constexpr int kBarPairA = kBarPeerFree + kRecvSlots;     // [4]
+// tile i uses TMEM region i % kRegions and barrier [i % kRegions] of each set
+constexpr int kBarSFull = kBarIdxEmpty + kIdxSlots;      // [kRegions] S(i) computed
+constexpr int kBarSFree = kBarSFull + kRegions;          // [kRegions] senders have read S(i)
+constexpr int kBarPFull = kBarSFree + kRegions;          // [kRegions] P(i) written
+constexpr int kBarPvDone = kBarPFull + kRegions;         // [kRegions] P(i).V accumulated
+// One receive buffer holds one column half at a time: column half c of tile i
+// lands as phase i of RecvFull[c]; once the four softmax warps of that half
+// have read it, phase i of PeerFree[c] (in the sending CTA) completes.  Every
+// waiter waits for phase i of a barrier whose phase i - 1 is already complete,
+// so the parity test is unambiguous.
+constexpr int kBarRecvFull = kBarPvDone + kRegions;      // [2]
+constexpr int kBarPeerFree = kBarRecvFull + 2;           // [2]
+constexpr int kBarPairA = kBarPeerFree + 2;              // [4]
 constexpr int kBarPairB = kBarPairA + 4;        // [4]
 constexpr int kBarQReady = kBarPairB + 4;
 constexpr int kBarFinal = kBarQReady + 1;
@@ -126,18 +127,21 @@ constexpr int kOffAbort = kOffTmemSlot + 4;
 constexpr int kOffZero = kOffAbort + 4;  // a zero the compiler cannot see (dependency anchor)
 constexpr int kSmemBytes = kOffZero + 4;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kOffStages % 1024 == 0 && kStageBytes % 1024 == 0 && kOffQRope % 512 == 0, "operand alignment");
-static_assert(kOffStaging % 16 == 0 && kRecvSlotBytes % 16 == 0, "bulk copy alignment");
+static_assert(kOffStages % 1024 == 0 && kStageBytes % 1024 == 0 && kOffQHalf % 1024 == 0 && kOffQRope % 512 == 0,
+              "operand alignment");
+static_assert(kOffStaging % 16 == 0 && kXchgBlockBytes % 16 == 0, "bulk copy alignment");
 static_assert(kOffBars % 8 == 0, "barrier alignment");
 
-// TMEM columns (512 allocated): O | region 0 | region 1 | Q latent half (bf16
-// pairs).  Tile i's score tile S(i) (64 fp32 columns) lands in region i % 2;
-// once it has been read out, P(i) overwrites it as P_hi (columns 0-31 of the
-// region) and P_lo (columns 32-63), each 64 bf16 keys per row.
+// TMEM columns (512 allocated): O | regions 0..2 | Q latent dims [0, 128) of
+// this CTA (bf16 pairs; dims [128, 256) are a shared-memory operand).  Tile
+// i's score tile S(i) (64 fp32 columns) lands in region i % 3; once it has
+// been read out, P(i) overwrites it as P_hi (columns 0-31 of the region) and
+// P_lo (columns 32-63), each 64 bf16 keys per row.
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;
-constexpr uint32_t kTmemRegion = 256;  // + 64 * (i % 2)
-constexpr uint32_t kTmemQ = 384;
+constexpr uint32_t kTmemRegion = 256;  // + 64 * (i % kRegions)
+constexpr uint32_t kTmemQ = 448;
+static_assert(kTmemRegion + 64 * kRegions <= kTmemQ && kTmemQ + 64 == kTmemCols, "TMEM layout");
 
 constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;
 
@@ -191,20 +195,34 @@ __device__ __forceinline__ float4 lds16f(uint32_t addr) {
                : "memory");
   return v;
 }
-// Exchange layout of a partial score tile (staging buffer and receive slots):
-// column half c (keys [32c, 32c + 32)) of all heads is one 16 KB block, head h
-// a 128-byte row in it, 16-byte unit k (keys 32c + 4k .. 32c + 4k + 3) of row h
-// at k ^ (h & 7), so a warp's 32 rows spread over all banks.  The 32 rows of a
-// TMEM lane quadrant form one contiguous 4 KB block per column half.
-__device__ __forceinline__ uint32_t xchg_offset(int h, int c, int k) {
-  return static_cast<uint32_t>(c * kXchgHalfBytes + h * 128 + ((k ^ (h & 7)) << 4));
+// Exchange layout of one column half (32 keys) of a partial score tile, in the
+// staging and receive buffers: head h is a 128-byte row, 16-byte unit k (keys
+// 4k .. 4k + 3 of the half) of row h at k ^ (h & 7), so a warp's 32 rows spread
+// over all banks; the 32 rows of a TMEM lane quadrant form one 4 KB block.
+__device__ __forceinline__ uint32_t xchg_offset(int h, int k) {
+  return static_cast<uint32_t>(h * 128 + ((k ^ (h & 7)) << 4));
 }
 
 // ------------------------------------------------------------------ index warp
 // Two index warps take alternate passes of kIdxBatch tiles (warp iw owns the
 // ring slots [kIdxBatch iw, kIdxBatch iw + kIdxBatch)), so two chains of
-// dependent loads (top-k entry, then block_table) are in flight at once.
-__device__ void index_role(const Params& p, const Ctx& c, int iw, int lane) {
+// dependent loads (top-k entry, then block_table) are in flight at once.  Each
+// warp loads the top-k entries of its next pass before it resolves the
+// current one.
+static_assert(kIdxBatch == 4, "two entries per lane per tile, four tiles per pass");
+
+// top-k entries of the pass starting at tile j0 (-1 beyond the list)
+__device__ __forceinline__ void index_load(const Params& p, const int32_t* tk, int j0, int lane, int (&idx)[8]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int e = (j0 + (q >> 1)) * kTileKeys + (q & 1) * 32 + lane;
+    idx[q] = (j0 + (q >> 1) < p.n_tiles && e < p.topk) ? __ldg(tk + e) : -1;
+  }
+}
+
+// `idx` holds the entries of this warp's first pass, loaded before the CTA's
+// set-up barrier.
+__device__ void index_role(const Params& p, const Ctx& c, int iw, int lane, int (&idx)[8]) {
   const int b = c.t / p.S1;
   const int act = __ldg(p.act_seqs + b);
   const int32_t* tk = p.topk_idx + static_cast<int64_t>(c.t) * p.topk;
@@ -217,35 +235,34 @@ __device__ void index_role(const Params& p, const Ctx& c, int iw, int lane) {
   bool bad = false;
   for (int j0 = iw * kIdxBatch; j0 < p.n_tiles; j0 += kIndexWarps * kIdxBatch) {
     const int nb = min(kIdxBatch, p.n_tiles - j0);
+    int blk[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const bool valid = idx[q] >= 0 && idx[q] < act;
+      const int slot = idx[q] >> 7;
+      blk[q] = (valid && slot < p.mbps) ? __ldg(bt + slot) : -1;
+    }
+    int nxt[8];
+    index_load(p, tk, j0 + kIndexWarps * kIdxBatch, lane, nxt);
     bool ok = true;
     for (int k = 0; k < nb && ok; ++k) {
       const int j = j0 + k;
       ok = warp_wait(c, kBarIdxEmpty + (j % kIdxSlots), ((j / kIdxSlots) & 1) ^ 1);
     }
     if (!ok) break;
-    static_assert(kIdxBatch == 4, "two entries per lane per tile, four tiles per pass");
-    int idx[8], blk[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int e = (j0 + (q >> 1)) * kTileKeys + (q & 1) * 32 + lane;
-      idx[q] = ((q >> 1) < nb && e < p.topk) ? __ldg(tk + e) : -1;
-    }
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const bool valid = idx[q] >= 0 && idx[q] < act;
-      const int slot = idx[q] >> 7;
-      blk[q] = (valid && slot < p.mbps) ? __ldg(bt + slot) : -1;
-      if (valid && (blk[q] < 0 || blk[q] >= p.num_blocks)) bad = true;
-    }
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       if ((q >> 1) >= nb) continue;
-      const bool valid = idx[q] >= 0 && idx[q] < act && blk[q] >= 0 && blk[q] < p.num_blocks;
-      const int j = j0 + (q >> 1);
+      const bool in_seq = idx[q] >= 0 && idx[q] < act;
+      const bool valid = in_seq && blk[q] >= 0 && blk[q] < p.num_blocks;
+      if (in_seq && !valid) bad = true;
       const int row = blk[q] * 128 + (idx[q] & 127);
-      rows[(j % kIdxSlots) * kTileKeys + (q & 1) * 32 + lane] = valid ? row : -1;
+
+      rows[((j0 + (q >> 1)) % kIdxSlots) * kTileKeys + (q & 1) * 32 + lane] = valid ? row : -1;
     }
     for (int k = 0; k < nb; ++k) mbar_arrive(c.bar(kBarIdxFull + ((j0 + k) % kIdxSlots)));
+#pragma unroll
+    for (int q = 0; q < 8; ++q) idx[q] = nxt[q];
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&g_mla_status, MLA_DEVICE_BAD_BLOCK);
 }
@@ -346,48 +363,52 @@ __device__ void gather_role(const Params& p, const Ctx& c, int gw, int lane) {
 
 // ------------------------------------------------------------------ sender warps
 // Copy the CTA's partial score tile (128 heads x 64 keys, fp32) into the
-// peer's receive slot: TMEM -> registers -> the local staging buffer, then
-// bulk copies by the TMA engine, so the CTA-to-CTA traffic never queues in
-// front of the softmax warps' shared-memory accesses.
+// peer's receive buffer, one column half at a time: TMEM -> registers -> the
+// local staging buffer, then bulk copies by the TMA engine, so the CTA-to-CTA
+// traffic never queues in front of the softmax warps' shared-memory accesses.
+// Column half 0 of tile j may be copied once the peer has read half 1 of tile
+// j - 1 out of the buffer, half 1 once it has read half 0 of tile j.
+__device__ __forceinline__ bool send_half(const Ctx& c, const uint32_t (&v)[32], int h, int q, int lane, int j,
+                                          int half, uint32_t stg, uint32_t dst, uint32_t rbar) {
+  if (lane == 0) bulk_wait_read_all();  // the previous copy has left the staging buffer
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < 8; ++k) sts16(stg + xchg_offset(h, k), make_uint4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]));
+  fence_proxy_async_smem();  // generic-proxy stores -> bulk-copy reads
+  __syncwarp();
+  bool ok = true;
+  if (lane == 0) {
+    if (half == 0 && j > 0) ok = mbar_wait<true>(c.bar(kBarPeerFree + 1), (j - 1) & 1, c.abort, kWaitLimitNs);
+    if (half == 1) ok = mbar_wait<true>(c.bar(kBarPeerFree + 0), j & 1, c.abort, kWaitLimitNs);
+    if (ok) {
+      const uint32_t blk = static_cast<uint32_t>(q) * kXchgBlockBytes;
+      bulk_copy_to_peer(dst + blk, stg + blk, kXchgBlockBytes, rbar);
+      bulk_commit();
+    }
+  }
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
 __device__ void sender_role(const Params& p, const Ctx& c, int q, int lane) {
   const int h = q * 32 + lane;
-  const uint32_t tS = c.tmem + (static_cast<uint32_t>(q * 32) << 16) + kTmemRegion;
+  const uint32_t tR = c.tmem + (static_cast<uint32_t>(q * 32) << 16) + kTmemRegion;
   const uint32_t peer = c.crank ^ 1u;
   const uint32_t stg = c.sbase + kOffStaging;
-  const uint32_t recv_remote = mapa_shared(c.sbase + kOffRecv, peer);
+  const uint32_t dst = mapa_shared(c.sbase + kOffRecv, peer);
+  const uint32_t rbar0 = mapa_shared(c.bar(kBarRecvFull + 0), peer);
+  const uint32_t rbar1 = mapa_shared(c.bar(kBarRecvFull + 1), peer);
   for (int j = 0; j < p.n_tiles; ++j) {
-    if (!warp_wait(c, kBarSFull + (j & 1), (j >> 1) & 1)) break;
+    const int r = j % kRegions;
+    if (!warp_wait(c, kBarSFull + r, (j / kRegions) & 1)) break;
     tc_fence_after();
     uint32_t a[32], b[32];
-    tmem_ld_32x32b_x32(tS + 64 * (j & 1), a);
-    tmem_ld_32x32b_x32(tS + 64 * (j & 1) + 32, b);
+    tmem_ld_32x32b_x32(tR + 64 * r, a);
+    tmem_ld_32x32b_x32(tR + 64 * r + 32, b);
     tmem_wait_ld();
     tc_fence_before();
-    mbar_arrive_relaxed(c.bar(kBarSFree + (j & 1)));  // the values are in registers (wait::ld)
-    if (lane == 0) bulk_wait_read_all();    // the previous tile has left the staging buffer
-    __syncwarp();
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      sts16(stg + xchg_offset(h, 0, k), make_uint4(a[4 * k], a[4 * k + 1], a[4 * k + 2], a[4 * k + 3]));
-      sts16(stg + xchg_offset(h, 1, k), make_uint4(b[4 * k], b[4 * k + 1], b[4 * k + 2], b[4 * k + 3]));
-    }
-    fence_proxy_async_smem();  // generic-proxy stores -> bulk-copy reads
-    __syncwarp();
-    const int slot = j % kRecvSlots, use = j / kRecvSlots;
-    bool ok = true;
-    if (lane == 0) {
-      if (use > 0) ok = mbar_wait<true>(c.bar(kBarPeerFree + slot), (use & 1) ^ 1, c.abort, kWaitLimitNs);
-      if (ok) {
-        const uint32_t rbar = mapa_shared(c.bar(kBarRecvFull + slot), peer);
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const uint32_t off = xchg_offset(q * 32, half, 0);
-          bulk_copy_to_peer(recv_remote + slot * kRecvSlotBytes + off, stg + off, kXchgBlockBytes, rbar);
-        }
-        bulk_commit();
-      }
-    }
-    if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+    mbar_arrive_relaxed(c.bar(kBarSFree + r));  // the values are in registers (wait::ld)
+    if (!send_half(c, a, h, q, lane, j, 0, stg, dst, rbar0)) break;
+    if (!send_half(c, b, h, q, lane, j, 1, stg, dst, rbar1)) break;
   }
   // the peer cannot leave before this CTA reaches its final cluster barrier,
   // which waits for these copies to complete
@@ -399,26 +420,48 @@ __device__ void sender_role(const Params& p, const Ctx& c, int q, int lane) {
 __device__ __forceinline__ void issue_s(const Ctx& c, int k) {
   constexpr uint32_t idesc = make_idesc_f16(128, 64, 1, 0, 0);
   const uint32_t qrope = c.sbase + kOffQRope;
+  const uint32_t qhalf = c.sbase + kOffQHalf;
   const uint32_t stage = c.sbase + kOffStages + (k % kStages) * kStageBytes;
   fence_proxy_async_smem();  // cp.async / st.shared data -> tensor-core reads
   tc_fence_after();
-  // S = Q_latent K_latent^T (A = Q in TMEM) + Q_rope K_rope^T (A = Q rope in smem)
+  // S = Q_latent K_latent^T (dims [0, 128): A = Q in TMEM; dims [128, 256): A = Q
+  // in smem) + Q_rope K_rope^T (A = Q rope in smem)
+  const uint32_t dS = c.tmem + kTmemRegion + 64 * (k % kRegions);
+#ifdef MLA_COMPACT_ISSUE
+  {
+    // descriptors advance by 32 bytes per K step and kChunkBytes per 64 dims
+    const uint64_t b0 = make_sdesc(stage, 16, 1024, kSwizzle128B);
+    const uint64_t a0 = make_sdesc(qhalf, 16, 1024, kSwizzle128B);
+#pragma unroll 1
+    for (int s = 0; s < 8; ++s)
+      umma_ts(dS, c.tmem + kTmemQ + 8 * s, b0 + static_cast<uint64_t>((s >> 2) * (kChunkBytes >> 4) + (s & 3) * 2), idesc,
+              s > 0 ? 1u : 0u);
+#pragma unroll 1
+    for (int s = 8; s < 16; ++s)
+      umma_ss(dS, a0 + static_cast<uint64_t>(((s - 8) >> 2) * (kQHalfBytes / 32) + ((s - 8) & 3) * 2),
+              b0 + static_cast<uint64_t>((s >> 2) * (kChunkBytes >> 4) + (s & 3) * 2), idesc, 1u);
+  }
+#else
 #pragma unroll
-  const uint32_t dS = c.tmem + kTmemRegion + 64 * (k & 1);
-  for (int s = 0; s < 16; ++s)
+  for (int s = 0; s < 8; ++s)
     umma_ts(dS, c.tmem + kTmemQ + 8 * s,
             make_sdesc(stage + (s >> 2) * kChunkBytes + (s & 3) * 32, 16, 1024, kSwizzle128B), idesc, s > 0 ? 1u : 0u);
+#pragma unroll
+  for (int s = 8; s < 16; ++s)
+    umma_ss(dS, make_sdesc(qhalf + ((s - 8) >> 2) * (kQHalfBytes / 2) + ((s - 8) & 3) * 32, 16, 1024, kSwizzle128B),
+            make_sdesc(stage + (s >> 2) * kChunkBytes + (s & 3) * 32, 16, 1024, kSwizzle128B), idesc, 1u);
+#endif
 #pragma unroll
   for (int s = 0; s < 2; ++s)
     umma_ss(dS, make_sdesc(qrope + s * 32, 16, 512, kSwizzle64B),
             make_sdesc(stage + 4 * kChunkBytes + s * 32, 16, 512, kSwizzle64B), idesc, 1u);
-  umma_commit(c.bar(kBarSFull + (k & 1)));
+  umma_commit(c.bar(kBarSFull + k % kRegions));
 }
 
 __device__ __forceinline__ void issue_pv(const Ctx& c, int i) {
   constexpr uint32_t idesc = make_idesc_f16(128, 256, 1, 0, 1);
   const uint32_t stage = c.sbase + kOffStages + (i % kStages) * kStageBytes;
-  const uint32_t aP = c.tmem + kTmemRegion + 64 * (i & 1);
+  const uint32_t aP = c.tmem + kTmemRegion + 64 * (i % kRegions);
   tc_fence_after();
   // O += P_hi . V, then O += P_lo . V (same V tile, 16 keys per instruction)
 #pragma unroll
@@ -426,13 +469,13 @@ __device__ __forceinline__ void issue_pv(const Ctx& c, int i) {
     umma_ts(c.tmem + kTmemO, aP + (s < 4 ? 0 : 32) + 8 * (s & 3),
             make_sdesc(stage + (s & 3) * 16 * 128, kChunkBytes, 1024, kSwizzle128B), idesc,
             (i > 0 || s > 0) ? 1u : 0u);
-  umma_commit(c.bar(kBarPvDone + (i & 1)));
+  umma_commit(c.bar(kBarPvDone + i % kRegions));
   umma_commit(c.bar(kBarEmpty + (i % kStages)));
 }
 
 // One thread polls both hand-offs and issues whichever is ready: P.V(kp) as
 // soon as the softmax has written P(kp), and S(ks) once its key tile has
-// landed and P.V(ks - 2) has released TMEM region ks % 2, so a stage is
+// landed and P.V(ks - 3) has released TMEM region ks % 3, so a stage is
 // released as early as the data allows and the softmax of one tile overlaps
 // with the P.V of the previous one.
 __device__ void mma_role(const Params& p, const Ctx& c) {
@@ -442,12 +485,12 @@ __device__ void mma_role(const Params& p, const Ctx& c) {
   uint32_t spins = 0;
   while (ok && kp < p.n_tiles) {
     bool progressed = false;
-    if (kp < ks && mbar_poll(c.bar(kBarPFull + (kp & 1)), (kp >> 1) & 1)) {
+    if (kp < ks && mbar_poll(c.bar(kBarPFull + kp % kRegions), (kp / kRegions) & 1)) {
       issue_pv(c, kp++);
       progressed = true;
     }
     if (ks < p.n_tiles && mbar_poll(c.bar(kBarFull + ks % kStages), (ks / kStages) & 1) &&
-        (ks < 2 || mbar_poll(c.bar(kBarPvDone + (ks & 1)), ((ks >> 1) & 1) ^ 1))) {
+        (ks < kRegions || mbar_poll(c.bar(kBarPvDone + ks % kRegions), ((ks / kRegions) & 1) ^ 1))) {
       issue_s(c, ks++);
       progressed = true;
     }
@@ -473,27 +516,38 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
   const int h = q * 32 + lane;     // head
   const int tid = warp * 32 + lane;
   const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-  const uint32_t tR = c.tmem + lane_off + kTmemRegion;  // + 64 * (i % 2)
+  const uint32_t tR = c.tmem + lane_off + kTmemRegion;  // + 64 * (i % kRegions)
   const uint32_t tO = c.tmem + lane_off + kTmemO + 128 * half;
-  const uint32_t tQ = c.tmem + lane_off + kTmemQ + 64 * half;
+  const uint32_t tQ = c.tmem + lane_off + kTmemQ;
   const bool live = h < p.n_q;
   const int64_t qrow = static_cast<int64_t>(c.t) * p.n_q + h;
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
   {
-    // Q latent: this thread stores dims [128 half, 128 half + 128) of the CTA's 256
+    // Q latent, dims [128 half, 128 half + 128) of the CTA's 256: the lower half
+    // goes to TMEM, the upper half to shared memory (128-byte swizzled rows of
+    // 64 dims, head h at row h of chunk (d - 128) / 64)
     const uint8_t* qn = reinterpret_cast<const uint8_t*>(p.q_nope) + (qrow * 512 + c.crank * 256 + half * 128) * 2;
+    if (half == 0) {
 #pragma unroll
-    for (int ch = 0; ch < 2; ++ch) {
-      uint32_t w[32];
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t w[32];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const uint4 v = live ? ldg16(qn + (ch * 8 + u) * 16) : zero;
-        w[4 * u + 0] = v.x;
-        w[4 * u + 1] = v.y;
-        w[4 * u + 2] = v.z;
-        w[4 * u + 3] = v.w;
+        for (int u = 0; u < 8; ++u) {
+          const uint4 v = live ? ldg16(qn + (ch * 8 + u) * 16) : zero;
+          w[4 * u + 0] = v.x;
+          w[4 * u + 1] = v.y;
+          w[4 * u + 2] = v.z;
+          w[4 * u + 3] = v.w;
+        }
+        tmem_st_32x32b_x32(tQ + 32 * ch, w);
       }
-      tmem_st_32x32b_x32(tQ + 32 * ch, w);
+    } else {
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          sts16(c.sbase + kOffQHalf + ch * (kQHalfBytes / 2) + h * 128 + ((u ^ (h & 7)) << 4),
+                live ? ldg16(qn + (ch * 8 + u) * 16) : zero);
     }
     // Q rope: this CTA's 32 dims [32 crank, 32 crank + 32), units 2 half, 2 half + 1
     const uint8_t* qr = reinterpret_cast<const uint8_t*>(p.q_rope) + (qrow * 64 + c.crank * 32 + half * 16) * 2;
@@ -518,22 +572,24 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
     {
       // own partial score tile i, read out at once so the next score MMA can
       // start while the peer's partial is still on its way
-      const uint32_t reg = tR + 64 * (i & 1);
-      if (!warp_wait(c, kBarSFull + (i & 1), (i >> 1) & 1)) { ok = false; break; }
+      const uint32_t reg = tR + 64 * (i % kRegions);
+      if (!warp_wait(c, kBarSFull + i % kRegions, (i / kRegions) & 1)) { ok = false; break; }
       tc_fence_after();
       uint32_t own[32];
       tmem_ld_32x32b_x32(reg + 32 * half, own);
       tmem_wait_ld();
       tc_fence_before();  // ordered before the row-max handshake that precedes P(i) stores
-      const int b = i % kRecvSlots;
-      if (!warp_wait_cluster(c, kBarRecvFull + b, (i / kRecvSlots) & 1)) { ok = false; break; }
-      if (tid == 0 && i + kRecvSlots < p.n_tiles) mbar_arrive_expect_tx(c.bar(kBarRecvFull + b), kRecvSlotBytes);
+      // the peer's partial for this warp's key columns (column half `half`)
+      if (!warp_wait_cluster(c, kBarRecvFull + half, i & 1)) { ok = false; break; }
+      // arm this half's next phase before the buffer is freed (the peer copies
+      // into it only after that), so each phase is armed exactly once
+      if (lane == 0 && q == 0 && i + 1 < p.n_tiles) mbar_arrive_expect_tx(c.bar(kBarRecvFull + half), kXchgBytes);
       float s[32];
-      const uint32_t slot = c.sbase + kOffRecv + b * kRecvSlotBytes;
+      const uint32_t slot = c.sbase + kOffRecv;
       uint32_t dep = 0;
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const float4 v = lds16f(slot + xchg_offset(h, half, k));
+        const float4 v = lds16f(slot + xchg_offset(h, k));
         s[4 * k + 0] = __uint_as_float(own[4 * k + 0]) + v.x;
         s[4 * k + 1] = __uint_as_float(own[4 * k + 1]) + v.y;
         s[4 * k + 2] = __uint_as_float(own[4 * k + 2]) + v.z;
@@ -543,7 +599,7 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
       // Free the slot for the peer.  The arrive's address depends on every
       // loaded value (dep & dep_zero, a run-time 0), so it cannot issue
       // before the loads have returned and needs no release fence.
-      mbar_arrive_remote_relaxed(mapa_shared(c.bar(kBarPeerFree + b), peer) + (dep & dep_zero));
+      mbar_arrive_remote_relaxed(mapa_shared(c.bar(kBarPeerFree + half), peer) + (dep & dep_zero));
       // mask (waiting on the stage barrier acquires the gather's validity bits) and scale
       if (!warp_wait(c, kBarFull + (i % kStages), (i / kStages) & 1)) { ok = false; break; }
       const uint32_t vm = static_cast<uint32_t>(vmask[i % kStages] >> (32 * half));
@@ -571,7 +627,7 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
       }
       if (__any_sync(0xffffffffu, grow) && i > 0) {
         // O may only be rescaled once P(i-1).V has been accumulated into it
-        if (!warp_wait(c, kBarPvDone + ((i - 1) & 1), ((i - 1) >> 1) & 1)) { ok = false; break; }
+        if (!warp_wait(c, kBarPvDone + (i - 1) % kRegions, ((i - 1) / kRegions) & 1)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {
@@ -601,13 +657,13 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
       // P(i) overwrites S(i) in its region: the senders must have read it out
       // (this warp and its pair partner read their own columns before the
       // row-max handshake above)
-      if (!warp_wait(c, kBarSFree + (i & 1), (i >> 1) & 1)) { ok = false; break; }
+      if (!warp_wait(c, kBarSFree + i % kRegions, (i / kRegions) & 1)) { ok = false; break; }
       tc_fence_after();
       tmem_st_32x32b_x16(reg + 16 * half, phi);
       tmem_st_32x32b_x16(reg + 32 + 16 * half, plo);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(c.bar(kBarPFull + (i & 1)));
+      mbar_arrive(c.bar(kBarPFull + i % kRegions));
     }
   }
   if (!ok) return;
@@ -616,7 +672,7 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
   mbar_arrive(c.bar(kBarPairA + q));
   if (!warp_wait(c, kBarPairA + q, p.n_tiles & 1)) return;
   const float l_tot = half == 0 ? l + pair[kHeads + h] : pair[h] + l;
-  if (!warp_wait(c, kBarPvDone + ((p.n_tiles - 1) & 1), ((p.n_tiles - 1) >> 1) & 1)) return;
+  if (!warp_wait(c, kBarPvDone + (p.n_tiles - 1) % kRegions, ((p.n_tiles - 1) / kRegions) & 1)) return;
   tc_fence_after();
   const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
   uint4* op = reinterpret_cast<uint4*>(p.out + qrow * 512 + c.crank * 256 + half * 128);
@@ -665,15 +721,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_spa
       mbar_init(c.bar(kBarIdxFull + i), 32);
       mbar_init(c.bar(kBarIdxEmpty + i), 256);
     }
-    for (int r = 0; r < 2; ++r) {
+    for (int r = 0; r < kRegions; ++r) {
       mbar_init(c.bar(kBarSFull + r), 1);
       mbar_init(c.bar(kBarSFree + r), kSenderThreads);
       mbar_init(c.bar(kBarPFull + r), kSoftmaxThreads);
       mbar_init(c.bar(kBarPvDone + r), 1);
     }
-    for (int b = 0; b < kRecvSlots; ++b) {
-      mbar_init(c.bar(kBarRecvFull + b), 1);
-      mbar_init(c.bar(kBarPeerFree + b), kSoftmaxThreads);
+    for (int h2 = 0; h2 < 2; ++h2) {
+      mbar_init(c.bar(kBarRecvFull + h2), 1);
+      mbar_init(c.bar(kBarPeerFree + h2), kSoftmaxThreads / 2);  // the four warps reading that column half
     }
     for (int q = 0; q < 4; ++q) {
       mbar_init(c.bar(kBarPairA + q), 64);
@@ -682,9 +738,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_spa
     mbar_init(c.bar(kBarQReady), kSoftmaxThreads);
     mbar_init(c.bar(kBarFinal), 1);
     fence_mbarrier_init_cluster();
-    for (int b = 0; b < kRecvSlots; ++b) mbar_arrive_expect_tx(c.bar(kBarRecvFull + b), kRecvSlotBytes);
+    for (int h2 = 0; h2 < 2; ++h2) mbar_arrive_expect_tx(c.bar(kBarRecvFull + h2), kXchgBytes);
     *reinterpret_cast<volatile uint32_t*>(smem + kOffZero) = 0u;
   }
+  // the index warps issue their first top-k loads before the set-up barrier
+  int idx0[8];
+  if (warp >= kIndexWarp && warp < kIndexWarp + kIndexWarps)
+    index_load(p, p.topk_idx + static_cast<int64_t>(c.t) * p.topk, (warp - kIndexWarp) * kIdxBatch, lane, idx0);
   if (warp == kMmaWarp) {
     tmem_alloc(c.sbase + kOffTmemSlot, kTmemCols);
     tmem_relinquish();
@@ -710,7 +770,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_spa
         if (lane == 0) mma_role(p, c);
         __syncwarp();
       } else if (warp < kIndexWarp + kIndexWarps) {
-        index_role(p, c, warp - kIndexWarp, lane);
+        index_role(p, c, warp - kIndexWarp, lane, idx0);
       }
     }
   }

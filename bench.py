@@ -114,6 +114,26 @@ def ncu_traffic(workload):
     return float(mt.group(1))
 
 
+SEEDS = {"tiny_decode": 0, "mtp_decode": 1, "int8_decode": 2, "varlen_decode": 3, "prefill": 4}
+
+
+def rank_seed(workload: str, rank: int) -> int:
+    """Every rank draws its own batch (weak scaling): the workload's seed plus 1000 per rank."""
+    return SEEDS[workload] + 1000 * rank
+
+
+def reduce_max_over_ranks(values, device):
+    """Element-wise maximum of a list of floats over all ranks (identity when
+    no process group is initialised)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
 def run_config(workload, d, world):
     """The ``config`` object of the JSON line (the same for both arms)."""
     return {
@@ -242,8 +262,7 @@ def main():
 
     # every rank draws its own batch (weak scaling)
     gen = workloads.NAMED[args.workload]
-    inp = gen(seed={"tiny_decode": 0, "mtp_decode": 1, "int8_decode": 2, "varlen_decode": 3,
-                    "prefill": 4}[args.workload] + 1000 * rank)
+    inp = gen(seed=rank_seed(args.workload, rank))
     counts = algorithmic_counts(inp)
     dev = workloads.to_device(inp)
     dims = mla.dims_from_workload(inp["dims"])
@@ -311,10 +330,7 @@ def main():
 
     us = float(np.mean(times_ms) * 1000.0)
     e2e_us = float(np.mean(e2e_ms) * 1000.0)
-    if world > 1:
-        t = torch.tensor([us, e2e_us], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        us, e2e_us = float(t[0]), float(t[1])
+    us, e2e_us = reduce_max_over_ranks([us, e2e_us], device="cuda")
 
     if rank == 0:
         hbm_gbs, bf16_tf, peak_src = measured_peaks()

@@ -35,9 +35,10 @@
  *     wait that runs out raises MLA_DEVICE_TIMEOUT (sticky: later launches do
  *     no work until the status is cleared).
  *   - Numerics: inputs bf16; products are exact; score and output
- *     accumulation in fp32 on the tensor cores; the softmax weights P and the
- *     values enter the P.V product as fp16 (exact conversion of bf16 values
- *     whose magnitude lies in [2^-14, 65504]); out is rounded to bf16 once.
+ *     accumulation in fp32 on the tensor cores; the softmax weights P enter
+ *     the P.V product as two bf16 terms, P_hi = bf16(p) and
+ *     P_lo = bf16(p - P_hi), so their relative error stays below 2^-18; the
+ *     values are the bf16 cache rows themselves; out is rounded to bf16 once.
  */
 #ifndef MLA_SPARSE_H_
 #define MLA_SPARSE_H_

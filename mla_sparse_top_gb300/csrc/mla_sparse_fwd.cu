@@ -427,21 +427,6 @@ __device__ __forceinline__ void issue_s(const Ctx& c, int k) {
   // S = Q_latent K_latent^T (dims [0, 128): A = Q in TMEM; dims [128, 256): A = Q
   // in smem) + Q_rope K_rope^T (A = Q rope in smem)
   const uint32_t dS = c.tmem + kTmemRegion + 64 * (k % kRegions);
-#ifdef MLA_COMPACT_ISSUE
-  {
-    // descriptors advance by 32 bytes per K step and kChunkBytes per 64 dims
-    const uint64_t b0 = make_sdesc(stage, 16, 1024, kSwizzle128B);
-    const uint64_t a0 = make_sdesc(qhalf, 16, 1024, kSwizzle128B);
-#pragma unroll 1
-    for (int s = 0; s < 8; ++s)
-      umma_ts(dS, c.tmem + kTmemQ + 8 * s, b0 + static_cast<uint64_t>((s >> 2) * (kChunkBytes >> 4) + (s & 3) * 2), idesc,
-              s > 0 ? 1u : 0u);
-#pragma unroll 1
-    for (int s = 8; s < 16; ++s)
-      umma_ss(dS, a0 + static_cast<uint64_t>(((s - 8) >> 2) * (kQHalfBytes / 32) + ((s - 8) & 3) * 2),
-              b0 + static_cast<uint64_t>((s >> 2) * (kChunkBytes >> 4) + (s & 3) * 2), idesc, 1u);
-  }
-#else
 #pragma unroll
   for (int s = 0; s < 8; ++s)
     umma_ts(dS, c.tmem + kTmemQ + 8 * s,
@@ -450,7 +435,6 @@ __device__ __forceinline__ void issue_s(const Ctx& c, int k) {
   for (int s = 8; s < 16; ++s)
     umma_ss(dS, make_sdesc(qhalf + ((s - 8) >> 2) * (kQHalfBytes / 2) + ((s - 8) & 3) * 32, 16, 1024, kSwizzle128B),
             make_sdesc(stage + (s >> 2) * kChunkBytes + (s & 3) * 32, 16, 1024, kSwizzle128B), idesc, 1u);
-#endif
 #pragma unroll
   for (int s = 0; s < 2; ++s)
     umma_ss(dS, make_sdesc(qrope + s * 32, 16, 512, kSwizzle64B),

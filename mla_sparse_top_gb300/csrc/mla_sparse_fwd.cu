@@ -99,7 +99,7 @@ constexpr int kOffQHalf = kOffStages + kStages * kStageBytes;
 constexpr int kOffQRope = kOffQHalf + kQHalfBytes;
 constexpr int kOffRows = kOffQRope + kQRopeBytes;       // int32 [kIdxSlots][64]
 constexpr int kOffPair = kOffRows + kIdxSlots * kTileKeys * 4;
-constexpr int kOffVmask = kOffPair + 2 * kHeads * 4;    // uint64 [kStages]
+constexpr int kOffVmask = kOffPair + 4 * kHeads * 4;    // uint64 [kStages]; the pair slots are float [2][2][kHeads]
 constexpr int kOffBars = kOffVmask + kStages * 8;
 constexpr int kBarFull = 0;
 constexpr int kBarEmpty = kBarFull + kStages;
@@ -118,8 +118,7 @@ constexpr int kBarPvDone = kBarPFull + kRegions;         // [kRegions] P(i).V ac
 constexpr int kBarRecvFull = kBarPvDone + kRegions;      // [2]
 constexpr int kBarPeerFree = kBarRecvFull + 2;           // [2]
 constexpr int kBarPairA = kBarPeerFree + 2;              // [4]
-constexpr int kBarPairB = kBarPairA + 4;        // [4]
-constexpr int kBarQReady = kBarPairB + 4;
+constexpr int kBarQReady = kBarPairA + 4;
 constexpr int kBarFinal = kBarQReady + 1;
 constexpr int kNumBars = kBarFinal + 1;
 constexpr int kOffTmemSlot = kOffBars + kNumBars * 8;
@@ -550,6 +549,11 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
   float* pair = reinterpret_cast<float*>(c.smem + kOffPair);
   const uint64_t* vmask = reinterpret_cast<const uint64_t*>(c.smem + kOffVmask);
   const float scl = p.scale_log2;
+  // scores enter exp2 as fma(s, mul, -m): the raw score times the scale for a
+  // positive scale (so the row max can be taken on raw scores), otherwise the
+  // score is scaled first and mul = 1
+  const bool raw_max = scl > 0.f;
+  const float mul = raw_max ? scl : 1.f;
   float m = -INFINITY, l = 0.f;
   bool ok = true;
   for (int i = 0; i < p.n_tiles; ++i) {
@@ -587,20 +591,25 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
       // mask (waiting on the stage barrier acquires the gather's validity bits) and scale
       if (!warp_wait(c, kBarFull + (i % kStages), (i / kStages) & 1)) { ok = false; break; }
       const uint32_t vm = static_cast<uint32_t>(vmask[i % kStages] >> (32 * half));
+      if (!raw_max) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) s[k] *= scl;
+      }
       float mx = -INFINITY;
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
-        s[k] = ((vm >> k) & 1u) ? s[k] * scl : -INFINITY;
+        s[k] = ((vm >> k) & 1u) ? s[k] : -INFINITY;
         mx = fmaxf(mx, s[k]);
       }
-      // row max across the two column halves of head h (bounded handshake
-      // between warps q and q + 4: post, both posted, read, both read)
-      pair[half * kHeads + h] = mx;
+      // Row max across the two column halves of head h: post, wait until both
+      // posted, read.  Tile i uses slot i % 2, so a slot is rewritten only two
+      // tiles later, after the partner has passed the next handshake (and so
+      // has read it).
+      float* slot_p = pair + (i & 1) * 2 * kHeads;
+      slot_p[half * kHeads + h] = mx;
       mbar_arrive(c.bar(kBarPairA + q));
       if (!warp_wait(c, kBarPairA + q, i & 1)) { ok = false; break; }
-      mx = fmaxf(mx, pair[(half ^ 1) * kHeads + h]);
-      mbar_arrive(c.bar(kBarPairB + q));
-      if (!warp_wait(c, kBarPairB + q, i & 1)) { ok = false; break; }
+      mx = fmaxf(mx, slot_p[(half ^ 1) * kHeads + h]) * mul;  // log2-scaled row max of the tile
       // Lazy rescale: m only moves when the tile max exceeds it by more than 8
       // (log2 units), so P stays below 2^8 and O is rescaled rarely.
       const bool grow = mx > m + 8.f;
@@ -629,8 +638,8 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
       float lsum = 0.f;
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
-        const float p0 = fast_exp2(s[2 * k] - mm);
-        const float p1 = fast_exp2(s[2 * k + 1] - mm);
+        const float p0 = fast_exp2(fmaf(s[2 * k], mul, -mm));
+        const float p1 = fast_exp2(fmaf(s[2 * k + 1], mul, -mm));
         lsum += p0 + p1;
         const uint32_t hw = pack_bf16x2(p0, p1);
         phi[k] = hw;
@@ -652,10 +661,11 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
   }
   if (!ok) return;
   // l over the whole row: add the partner's column half (same order in both threads)
-  pair[half * kHeads + h] = l;
+  float* slot_l = pair + (p.n_tiles & 1) * 2 * kHeads;
+  slot_l[half * kHeads + h] = l;
   mbar_arrive(c.bar(kBarPairA + q));
   if (!warp_wait(c, kBarPairA + q, p.n_tiles & 1)) return;
-  const float l_tot = half == 0 ? l + pair[kHeads + h] : pair[h] + l;
+  const float l_tot = half == 0 ? l + slot_l[kHeads + h] : slot_l[h] + l;
   if (!warp_wait(c, kBarPvDone + (p.n_tiles - 1) % kRegions, ((p.n_tiles - 1) / kRegions) & 1)) return;
   tc_fence_after();
   const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
@@ -715,10 +725,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_spa
       mbar_init(c.bar(kBarRecvFull + h2), 1);
       mbar_init(c.bar(kBarPeerFree + h2), kSoftmaxThreads / 2);  // the four warps reading that column half
     }
-    for (int q = 0; q < 4; ++q) {
-      mbar_init(c.bar(kBarPairA + q), 64);
-      mbar_init(c.bar(kBarPairB + q), 64);
-    }
+    for (int q = 0; q < 4; ++q) mbar_init(c.bar(kBarPairA + q), 64);
     mbar_init(c.bar(kBarQReady), kSoftmaxThreads);
     mbar_init(c.bar(kBarFinal), 1);
     fence_mbarrier_init_cluster();

@@ -219,11 +219,10 @@ __device__ __forceinline__ void index_load(const Params& p, const int32_t* tk, i
   }
 }
 
-// `idx` holds the entries of this warp's first pass, loaded before the CTA's
-// set-up barrier.
-__device__ void index_role(const Params& p, const Ctx& c, int iw, int lane, int (&idx)[8]) {
+// `idx` holds the entries of this warp's first pass and `act` the token's
+// sequence length, both loaded before the CTA's set-up barrier.
+__device__ void index_role(const Params& p, const Ctx& c, int iw, int lane, int (&idx)[8], int act) {
   const int b = c.t / p.S1;
-  const int act = __ldg(p.act_seqs + b);
   const int32_t* tk = p.topk_idx + static_cast<int64_t>(c.t) * p.topk;
   const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.mbps;
   int32_t* rows = reinterpret_cast<int32_t*>(c.smem + kOffRows);
@@ -237,9 +236,10 @@ __device__ void index_role(const Params& p, const Ctx& c, int iw, int lane, int 
     int blk[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      const bool valid = idx[q] >= 0 && idx[q] < act;
+      // the table entry is loaded for any index inside the table (without
+      // waiting for the length check); entries outside [0, act) are dropped below
       const int slot = idx[q] >> 7;
-      blk[q] = (valid && slot < p.mbps) ? __ldg(bt + slot) : -1;
+      blk[q] = (idx[q] >= 0 && slot < p.mbps) ? __ldg(bt + slot) : -1;
     }
     int nxt[8];
     index_load(p, tk, j0 + kIndexWarps * kIdxBatch, lane, nxt);
@@ -733,9 +733,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_spa
     *reinterpret_cast<volatile uint32_t*>(smem + kOffZero) = 0u;
   }
   // the index warps issue their first top-k loads before the set-up barrier
-  int idx0[8];
-  if (warp >= kIndexWarp && warp < kIndexWarp + kIndexWarps)
+  int idx0[8], act0 = 0;
+  if (warp >= kIndexWarp && warp < kIndexWarp + kIndexWarps) {
+    act0 = __ldg(p.act_seqs + c.t / p.S1);
     index_load(p, p.topk_idx + static_cast<int64_t>(c.t) * p.topk, (warp - kIndexWarp) * kIdxBatch, lane, idx0);
+  }
   if (warp == kMmaWarp) {
     tmem_alloc(c.sbase + kOffTmemSlot, kTmemCols);
     tmem_relinquish();
@@ -761,7 +763,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_spa
         if (lane == 0) mma_role(p, c);
         __syncwarp();
       } else if (warp < kIndexWarp + kIndexWarps) {
-        index_role(p, c, warp - kIndexWarp, lane, idx0);
+        index_role(p, c, warp - kIndexWarp, lane, idx0, act0);
       }
     }
   }

@@ -1,10 +1,11 @@
-"""TEST INFRASTRUCTURE ONLY: the fp64 CPU oracle for sparse MLA attention.
+"""TEST INFRASTRUCTURE ONLY: the fp64 CPU oracle for sparse MLA attention and
+for the Lightning Indexer's top-k selection.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
 leg may import this package.  The CUDA product path never imports it and the
-two share no code.  The arithmetic lives in ``mla_oracle.c`` (see its header
-for the passages it follows); this module only compiles it and marshals numpy
-arrays through ctypes.
+two share no code.  The arithmetic lives in ``mla_oracle.c`` and
+``indexer_oracle.c`` (see their headers for the passages they follow); this
+module only compiles them and marshals numpy arrays through ctypes.
 """
 from __future__ import annotations
 
@@ -15,16 +16,16 @@ import subprocess
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "mla_oracle.c")
+_SRCS = [os.path.join(_HERE, "mla_oracle.c"), os.path.join(_HERE, "indexer_oracle.c")]
 _LIB_PATH = os.path.join(_HERE, "libmla_oracle.so")
 _lib = None
 
 
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc (fp contraction off, no fast-math)."""
-    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < max(map(os.path.getmtime, _SRCS)):
         cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
-               "-shared", "-fPIC", "-o", _LIB_PATH, _SRC, "-lm"]
+               "-shared", "-fPIC", "-o", _LIB_PATH] + _SRCS + ["-lm"]
         subprocess.run(cmd, check=True)
     return _LIB_PATH
 
@@ -43,6 +44,10 @@ def _load():
         lib.mla_oracle_dequant_rows.restype = None
         lib.mla_oracle_max_threads.argtypes = []
         lib.mla_oracle_max_threads.restype = I
+        lib.idx_oracle_scores.argtypes = [I] * 7 + [P] * 5 + [I, P, I, ctypes.POINTER(ctypes.c_int64)]
+        lib.idx_oracle_scores.restype = I
+        lib.idx_oracle_select.argtypes = [I, I, P, I, P, I, P]
+        lib.idx_oracle_select.restype = I
         _lib = lib
     return _lib
 
@@ -103,4 +108,41 @@ def dequant_rows(q8: np.ndarray, scales: np.ndarray) -> np.ndarray:
     rows, d_nope = q8.shape
     out = np.empty((rows, d_nope), dtype=np.uint16)
     lib.mla_oracle_dequant_rows(_ptr(q8), _ptr(scales), rows, d_nope, _ptr(out))
+    return out
+
+
+# ------------------------------------------------------------------ Lightning Indexer
+def indexer_scores(inp: dict, threads: int = 0):
+    """Exact index scores I[t, j] (fp64, (T, ld) with ld = max_blocks_per_seq *
+    block_size); -inf where j is not a candidate.  Returns (scores, bad_blocks)."""
+    lib = _load()
+    d = inp["dims"]
+    T = d["B"] * d["S1"]
+    ld = d["max_blocks_per_seq"] * d["block_size"]
+    scores = np.empty((T, ld), dtype=np.float64)
+    bad = ctypes.c_int64(0)
+    rc = lib.idx_oracle_scores(d["B"], d["S1"], d["n_heads"], d["head_dim"], d["block_size"], d["num_blocks"],
+                               d["max_blocks_per_seq"],
+                               _ptr(np.ascontiguousarray(inp["q"], dtype=np.uint16)),
+                               _ptr(np.ascontiguousarray(inp["w"], dtype=np.float32)),
+                               _ptr(np.ascontiguousarray(inp["k_cache"], dtype=np.uint16)),
+                               _ptr(np.ascontiguousarray(inp["block_table"], dtype=np.int32)),
+                               _ptr(np.ascontiguousarray(inp["act_seqs"], dtype=np.int32)),
+                               ld, _ptr(scores), threads, ctypes.byref(bad))
+    if rc != 0:
+        raise ValueError(f"idx_oracle_scores rejected the arguments ({rc})")
+    return scores, int(bad.value)
+
+
+def indexer_select(scores, act_seqs, S1: int, topk: int):
+    """The selection rule on any scores array (converted exactly to fp64):
+    (T, topk) int32, ascending positions, -1 padded."""
+    lib = _load()
+    sc = np.ascontiguousarray(np.asarray(scores, dtype=np.float64))
+    act = np.ascontiguousarray(act_seqs, dtype=np.int32)
+    T, ld = sc.shape
+    out = np.empty((T, topk), dtype=np.int32)
+    rc = lib.idx_oracle_select(T // S1, S1, _ptr(act), ld, _ptr(sc), topk, _ptr(out))
+    if rc != 0:
+        raise ValueError(f"idx_oracle_select rejected the arguments ({rc})")
     return out

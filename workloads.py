@@ -200,3 +200,91 @@ def to_device(inp: dict, device="cuda") -> dict:
     dev["out"] = torch.empty((T, H, d["d_nope"]), dtype=torch.bfloat16, device=device)
     dev["lse"] = torch.empty((T, H), dtype=torch.float32, device=device)
     return dev
+
+
+# ------------------------------------------------------------------ Lightning Indexer inputs
+INDEXER_HEADS = 64
+INDEXER_DIM = 128
+
+
+def make_indexer_inputs(*, B: int, S1: int, act_seqs, topk: int, seed: int, n_heads: int = INDEXER_HEADS,
+                        head_dim: int = INDEXER_DIM, num_blocks: int | None = None,
+                        max_blocks_per_seq: int | None = None, poison_unused: bool = True,
+                        w_scale: float = 1.0, name: str = "custom") -> dict:
+    """One Lightning Indexer workload: q (B*S1, H, D) bf16 ~ N(0, 1), the
+    per-token head weights w (B*S1, H) fp32 ~ N(0, w_scale^2), and a paged
+    index-key cache k_cache (num_blocks*128, D) bf16 ~ N(0, 1) with the same
+    block-table construction as make_inputs (rows no candidate can reach are
+    NaN when ``poison_unused``)."""
+    g = torch.Generator().manual_seed(int(seed))
+    act = np.asarray(act_seqs, dtype=np.int64).reshape(B)
+    nb = [(int(a) + BLOCK_SIZE - 1) // BLOCK_SIZE for a in act]
+    used = int(sum(nb))
+    if num_blocks is None:
+        num_blocks = max(used, 1)
+    if max_blocks_per_seq is None:
+        max_blocks_per_seq = max(max(nb), 1)
+    perm = torch.randperm(num_blocks, generator=g).numpy().astype(np.int32)
+    block_table = np.full((B, max_blocks_per_seq), -1, dtype=np.int32)
+    o = 0
+    for b in range(B):
+        block_table[b, : nb[b]] = perm[o:o + nb[b]]
+        o += nb[b]
+    T = B * S1
+    k_cache = _randn_bf16(g, (num_blocks * BLOCK_SIZE, head_dim))
+    q = _randn_bf16(g, (T, n_heads, head_dim))
+    w = (torch.randn((T, n_heads), generator=g) * w_scale).to(torch.float32).numpy()
+    if poison_unused:
+        reach = np.zeros(num_blocks * BLOCK_SIZE, dtype=bool)
+        for b in range(B):
+            for s in range(nb[b]):
+                lo = block_table[b, s] * BLOCK_SIZE
+                reach[lo:lo + min(BLOCK_SIZE, int(act[b]) - s * BLOCK_SIZE)] = True
+        k_cache[~reach] = BF16_NAN_BITS
+    dims = dict(B=B, S1=S1, n_heads=n_heads, head_dim=head_dim, block_size=BLOCK_SIZE, num_blocks=int(num_blocks),
+                max_blocks_per_seq=int(max_blocks_per_seq), topk=int(topk))
+    return dict(name=name, dims=dims, q=q, w=w, k_cache=k_cache, block_table=block_table,
+                act_seqs=act.astype(np.int32))
+
+
+def indexer_decode(seed: int = 5, B: int = 64) -> dict:
+    """B=64 S1=2, 64 heads x 128 dims, act 8192 each over 4096 shuffled blocks, top-2048."""
+    return make_indexer_inputs(B=B, S1=2, act_seqs=[8192] * B, topk=2048, seed=seed, name="indexer_decode")
+
+
+def indexer_tiny(seed: int = 6) -> dict:
+    """B=1 S1=1, 8 heads, act 300 (3 of 5 blocks, the last partial), top-64."""
+    return make_indexer_inputs(B=1, S1=1, n_heads=8, act_seqs=[300], topk=64, num_blocks=5, seed=seed,
+                               name="indexer_tiny")
+
+
+def indexer_varlen(seed: int = 7, B: int = 8) -> dict:
+    """B=8 S1=2, act_b ~ U{100..20000} (some below top-k), top-2048."""
+    g = torch.Generator().manual_seed(int(seed) + 1000)
+    act = torch.randint(100, 20001, (B,), generator=g).numpy()
+    return make_indexer_inputs(B=B, S1=2, act_seqs=act, topk=2048, seed=seed, name="indexer_varlen")
+
+
+INDEXER_NAMED = {
+    "indexer_tiny": indexer_tiny,
+    "indexer_decode": indexer_decode,
+    "indexer_varlen": indexer_varlen,
+}
+
+
+def indexer_to_device(inp: dict, device="cuda") -> dict:
+    """Copy an indexer workload to the device, plus empty topk / scores outputs."""
+    d = inp["dims"]
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+    def raw(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+    T = d["B"] * d["S1"]
+    dev = dict(q=bf(inp["q"]), w=raw(inp["w"]), k_cache=bf(inp["k_cache"]), block_table=raw(inp["block_table"]),
+               act_seqs=raw(inp["act_seqs"]))
+    dev["topk_idx"] = torch.empty((T, d["topk"]), dtype=torch.int32, device=device)
+    dev["scores"] = torch.empty((T, d["max_blocks_per_seq"] * d["block_size"]), dtype=torch.float32, device=device)
+    return dev

@@ -1,4 +1,4 @@
-"""ctypes binding of the C ABI in include/mla_sparse.h.
+"""ctypes binding of the C ABI in include/mla_sparse.h and include/mla_indexer.h.
 
 Argument marshalling only: shapes and dtypes are read off torch tensors, the
 device pointers and the current CUDA stream are passed through, and a
@@ -25,13 +25,19 @@ MLA_DEVICE_BAD_BLOCK = 0x1
 MLA_DEVICE_TIMEOUT = 0x2
 
 EXPORTED_SYMBOLS = ("mla_sparse_attn_fwd", "mla_sparse_last_error", "mla_sparse_device_status",
-                    "mla_sparse_abi_version")
+                    "mla_sparse_abi_version", "mla_indexer_workspace_bytes", "mla_indexer_topk",
+                    "mla_indexer_device_status", "mla_indexer_last_error")
 
 
 class MlaDims(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int32) for name in (
         "B", "S1", "n_q", "n_kv", "d_nope", "d_rope", "block_size", "num_blocks", "max_blocks_per_seq",
         "topk", "kv_dtype")]
+
+
+class IndexerDims(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_int32) for name in (
+        "B", "S1", "n_heads", "head_dim", "block_size", "num_blocks", "max_blocks_per_seq", "topk")]
 
 
 class MlaError(RuntimeError):
@@ -60,6 +66,14 @@ def load_library(path: str = LIB_PATH):
     lib.mla_sparse_device_status.restype = ctypes.c_int
     lib.mla_sparse_abi_version.argtypes = []
     lib.mla_sparse_abi_version.restype = ctypes.c_int32
+    lib.mla_indexer_workspace_bytes.argtypes = [ctypes.POINTER(IndexerDims)]
+    lib.mla_indexer_workspace_bytes.restype = ctypes.c_size_t
+    lib.mla_indexer_topk.argtypes = [ctypes.POINTER(IndexerDims)] + [vp] * 7 + [ctypes.c_size_t, vp]
+    lib.mla_indexer_topk.restype = ctypes.c_int
+    lib.mla_indexer_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int32]
+    lib.mla_indexer_device_status.restype = ctypes.c_int
+    lib.mla_indexer_last_error.argtypes = []
+    lib.mla_indexer_last_error.restype = ctypes.c_char_p
     _lib = lib
     return lib
 
@@ -134,3 +148,43 @@ def device_status(clear: bool = True, stream=None) -> int:
 
 def abi_version() -> int:
     return int(load_library().mla_sparse_abi_version())
+
+
+# ------------------------------------------------------------------ Lightning Indexer
+def _check_idx(status: int):
+    if status != MLA_OK:
+        raise MlaError(status, load_library().mla_indexer_last_error().decode())
+
+
+def indexer_dims_from_workload(d: dict) -> IndexerDims:
+    return IndexerDims(**{f: int(d[f]) for f, _ in IndexerDims._fields_})
+
+
+def mla_indexer_workspace_bytes(dims: IndexerDims) -> int:
+    return int(load_library().mla_indexer_workspace_bytes(ctypes.byref(dims)))
+
+
+def mla_indexer_topk(q, w, k_cache, block_table, act_seqs, topk_idx, workspace, *, dims: IndexerDims, stream=None):
+    """Enqueue one call of the C entry point with the same name.
+
+    q (B*S1, H, 128) bf16, w (B*S1, H) fp32, k_cache (rows, 128) bf16,
+    block_table (B, W) int32, act_seqs (B,) int32, topk_idx (B*S1, topk) int32
+    (output), workspace: a device tensor of at least
+    mla_indexer_workspace_bytes(dims) bytes (holds the fp32 scores [B*S1, W*128]
+    on return).
+    """
+    lib = load_library()
+    nbytes = workspace.numel() * workspace.element_size()
+    st = lib.mla_indexer_topk(ctypes.byref(dims), _ptr(q), _ptr(w), _ptr(k_cache), _ptr(block_table), _ptr(act_seqs),
+                              _ptr(topk_idx), _ptr(workspace), ctypes.c_size_t(nbytes), _stream_handle(stream))
+    _check_idx(st)
+    return topk_idx
+
+
+def indexer_device_status(clear: bool = True, stream=None) -> int:
+    lib = load_library()
+    flags = ctypes.c_uint32(0)
+    st = lib.mla_indexer_device_status(_stream_handle(stream), ctypes.byref(flags), 1 if clear else 0)
+    if st not in (MLA_OK, -7):
+        _check_idx(st)
+    return int(flags.value)

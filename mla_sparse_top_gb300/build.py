@@ -7,11 +7,12 @@ import subprocess
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
-SOURCES = [os.path.join(CSRC, "mla_sparse_fwd.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, "ptx.cuh"), os.path.join(ROOT, "include", "mla_sparse.h")]
+SOURCES = [os.path.join(CSRC, "mla_sparse_fwd.cu"), os.path.join(CSRC, "lightning_indexer.cu")]
+DEPS = SOURCES + [os.path.join(CSRC, "ptx.cuh"), os.path.join(ROOT, "include", "mla_sparse.h"),
+                  os.path.join(ROOT, "include", "mla_indexer.h")]
 LIB_PATH = os.path.join(HERE, "libmla_sparse.so")
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
-              "-Xcompiler", "-fPIC", "-shared"]
+              "-Xcompiler", "-fPIC", "-shared", "--threads", "2"]
 
 
 def nvcc() -> str:

@@ -1,6 +1,6 @@
 """Host-side checks of the C ABI: the library builds, loads, exports every
-function include/mla_sparse.h declares, and rejects bad arguments before
-touching the GPU (every case below fails validation, so no CUDA call runs)."""
+function include/*.h declares, and rejects bad arguments before touching the
+GPU (every case below fails validation, so no CUDA call runs)."""
 import ctypes
 import os
 import re
@@ -8,7 +8,7 @@ import re
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "mla_sparse.h")
+HEADERS = [os.path.join(ROOT, "include", "mla_sparse.h"), os.path.join(ROOT, "include", "mla_indexer.h")]
 
 
 @pytest.fixture(scope="module")
@@ -19,15 +19,18 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(mla_sparse_\w+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(mla_(?:sparse|indexer)_\w+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
     assert {"mla_sparse_attn_fwd", "mla_sparse_last_error", "mla_sparse_device_status",
-            "mla_sparse_abi_version"} <= set(names)
+            "mla_sparse_abi_version", "mla_indexer_topk", "mla_indexer_workspace_bytes",
+            "mla_indexer_device_status", "mla_indexer_last_error"} <= set(names)
 
 
 def test_library_exports_every_declared_function(lib):
@@ -113,3 +116,58 @@ def test_binding_fails_loudly_without_library(tmp_path):
             binding.load_library(str(tmp_path / "missing.so"))
         finally:
             binding._lib = saved
+
+
+# ------------------------------------------------------------------ Lightning Indexer
+def _idims(**kw):
+    from mla_sparse_top_gb300.binding import IndexerDims
+    d = dict(B=2, S1=2, n_heads=64, head_dim=128, block_size=128, num_blocks=16, max_blocks_per_seq=8, topk=64)
+    d.update(kw)
+    return IndexerDims(**d)
+
+
+def test_indexer_workspace_size(lib):
+    d = _idims()
+    assert lib.mla_indexer_workspace_bytes(ctypes.byref(d)) == 2 * 2 * 8 * 128 * 4
+    assert lib.mla_indexer_workspace_bytes(ctypes.byref(_idims(n_heads=24))) == 0
+    assert lib.mla_indexer_workspace_bytes(None) == 0
+
+
+@pytest.mark.parametrize("case,expect", [
+    ("null_dims", -1), ("null_q", -1), ("null_ws", -1), ("heads_24", -4), ("heads_x_s1_big", -4), ("dim_64", -4),
+    ("block_64", -4), ("topk_zero", -2), ("batch_zero", -2), ("ws_small", -2), ("misaligned_q", -5),
+    ("misaligned_ws", -5),
+])
+def test_indexer_argument_errors_are_reported_before_launch(lib, case, expect):
+    d = _idims()
+    ptr = [ctypes.c_void_p(0x100000 * (i + 1)) for i in range(7)]
+    q, w, k, bt, act, topk, ws = ptr
+    ws_bytes = 2 * 2 * 8 * 128 * 4
+    dims = ctypes.byref(d)
+    if case == "null_dims":
+        dims = None
+    elif case == "null_q":
+        q = None
+    elif case == "null_ws":
+        ws = None
+    elif case == "heads_24":
+        d.n_heads = 24
+    elif case == "heads_x_s1_big":
+        d.n_heads, d.S1 = 256, 2
+    elif case == "dim_64":
+        d.head_dim = 64
+    elif case == "block_64":
+        d.block_size = 64
+    elif case == "topk_zero":
+        d.topk = 0
+    elif case == "batch_zero":
+        d.B = 0
+    elif case == "ws_small":
+        ws_bytes -= 4
+    elif case == "misaligned_q":
+        q = ctypes.c_void_p(0x100008)
+    elif case == "misaligned_ws":
+        ws = ctypes.c_void_p(0x100080)
+    st = lib.mla_indexer_topk(dims, q, w, k, bt, act, topk, ws, ctypes.c_size_t(ws_bytes), None)
+    assert st == expect, (case, st, lib.mla_indexer_last_error())
+    assert lib.mla_indexer_last_error()

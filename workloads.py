@@ -253,8 +253,8 @@ def indexer_decode(seed: int = 5, B: int = 64) -> dict:
 
 
 def indexer_tiny(seed: int = 6) -> dict:
-    """B=1 S1=1, 8 heads, act 300 (3 of 5 blocks, the last partial), top-64."""
-    return make_indexer_inputs(B=1, S1=1, n_heads=8, act_seqs=[300], topk=64, num_blocks=5, seed=seed,
+    """B=1 S1=1, 16 heads, act 300 (3 of 5 blocks, the last partial), top-64."""
+    return make_indexer_inputs(B=1, S1=1, n_heads=16, act_seqs=[300], topk=64, num_blocks=5, seed=seed,
                                name="indexer_tiny")
 
 

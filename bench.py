@@ -5,6 +5,11 @@ every batch entry, 4096 shuffled 128-row blocks, bf16 cache (seeded synthetic
 N(0,1) data).  One step = one call of the fused kernel over the whole batch.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+``--workload indexer_decode`` (or another indexer workload) times the
+Lightning Indexer + top-k instead: B=64 S1=2, 64 heads x 128 dims, 8192 keys
+per sequence, top-2048; one step = the score kernel then the selection kernel.
 
 Prints one JSON line (rank 0).  ``value`` is microseconds per call (the
 device-timed kernel, CUDA events on the launching stream, L2 flushed by a
@@ -46,7 +51,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="mtp_decode", choices=sorted(workloads.NAMED))
+    ap.add_argument("--workload", default="mtp_decode",
+                    choices=sorted(workloads.NAMED) + sorted(workloads.INDEXER_NAMED))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
     return ap.parse_args()
@@ -92,29 +98,33 @@ def measured_peaks():
         return 6800.0, 1900.0, "fallback"
 
 
-def kernel_source_hash():
+INDEXER_SOURCE = os.path.join(ROOT, "mla_sparse_top_gb300", "csrc", "lightning_indexer.cu")
+
+
+def kernel_source_hash(source=KERNEL_SOURCE):
     h = hashlib.sha256()
-    for fn in (KERNEL_SOURCE, os.path.join(ROOT, "mla_sparse_top_gb300", "csrc", "ptx.cuh")):
+    for fn in (source, os.path.join(ROOT, "mla_sparse_top_gb300", "csrc", "ptx.cuh")):
         with open(fn, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload):
+def ncu_traffic(workload, kernel=KERNEL_NAME, source=KERNEL_SOURCE):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel source (otherwise None)."""
-    fn = os.path.join(ROOT, "profiles", f"{KERNEL_NAME}_{workload}.md")
+    fn = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(fn):
         return None
     text = open(fn).read()
     mh = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
     mt = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not mh or not mt or mh.group(1) != kernel_source_hash():
+    if not mh or not mt or mh.group(1) != kernel_source_hash(source):
         return None
     return float(mt.group(1))
 
 
-SEEDS = {"tiny_decode": 0, "mtp_decode": 1, "int8_decode": 2, "varlen_decode": 3, "prefill": 4}
+SEEDS = {"tiny_decode": 0, "mtp_decode": 1, "int8_decode": 2, "varlen_decode": 3, "prefill": 4,
+         "indexer_decode": 5, "indexer_tiny": 6, "indexer_varlen": 7}
 
 
 def rank_seed(workload: str, rank: int) -> int:
@@ -142,8 +152,22 @@ def run_config(workload, d, world):
         "B": d["B"], "S1": d["S1"], "n_q": d["n_q"], "topk": d["topk"],
         "kv_dtype": "int8" if d["kv_int8"] else "bf16",
         "l2": "flushed between timed calls by a 256 MiB write (outside the per-call events)",
+        "launch": "a bounded GPU spin precedes each timed call, so its events time the device, not the host launch",
         "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
     }
+
+
+# ------------------------------------------------------------------ timing helpers
+SPIN_CYCLES = 400_000  # about 0.2 ms of GPU time
+
+
+def spin_gpu():
+    """A bounded GPU spin (torch's sleep kernel) enqueued after the L2 flush, so
+    that the host has enqueued the timed launch before its start event fires:
+    the per-call events then measure device time, not the host's launch cost
+    (which ``e2e`` includes)."""
+    import torch
+    torch.cuda._sleep(SPIN_CYCLES)
 
 
 # ------------------------------------------------------------------ clocks
@@ -247,7 +271,11 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
     if args.impl == "reference":
+        if args.workload in workloads.INDEXER_NAMED:
+            return run_reference_indexer(args, world, rank)
         return run_reference(args, world, rank)
+    if args.workload in workloads.INDEXER_NAMED:
+        return main_indexer(args, world, rank, local_rank)
 
     import torch
     import torch.distributed as dist
@@ -293,6 +321,7 @@ def main():
     clocks.mark_on()
     for i in range(args.steps):
         flush.fill_(float(i))
+        spin_gpu()
         starts[i].record(stream)
         launch()
         ends[i].record(stream)
@@ -383,6 +412,254 @@ def main():
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ Lightning Indexer + top-k
+INDEXER_METRIC = "Lightning Indexer + top-k µs/call, % HBM roofline of the score kernel (B64 S1=2 H64 topk2048)"
+INDEXER_KERNELS = ("idx_scores_kernel", "idx_topk_kernel")
+
+
+def indexer_counts(inp):
+    """Algorithmic bytes and flops of each of the two kernels, from the inputs:
+    the score kernel reads every candidate key row once (128 bf16), q, w and
+    the tables, and writes one fp32 score per (token, position); the selection
+    kernel reads those scores once and writes topk indices per token."""
+    d = inp["dims"]
+    T, H, D = d["B"] * d["S1"], d["n_heads"], d["head_dim"]
+    act = np.minimum(inp["act_seqs"].astype(np.int64), d["max_blocks_per_seq"] * d["block_size"])
+    keys = int(act.sum())
+    tok_keys = int(np.repeat(act, d["S1"]).sum())
+    tables = inp["block_table"].nbytes + inp["act_seqs"].nbytes
+    scores_bytes = keys * D * 2 + T * H * D * 2 + T * H * 4 + tables + tok_keys * 4
+    select_bytes = tok_keys * 4 + T * d["topk"] * 4 + inp["act_seqs"].nbytes
+    flops = 2.0 * tok_keys * H * D + 2.0 * tok_keys * H
+    return {"idx_scores_kernel": dict(bytes=scores_bytes, flops=flops),
+            "idx_topk_kernel": dict(bytes=select_bytes, flops=0.0)}
+
+
+def indexer_config(workload, d, world):
+    return {
+        "workload": f"{workload}: B={d['B']} S1={d['S1']} H={d['n_heads']} D={d['head_dim']} topk={d['topk']} "
+                    f"bf16 paged key cache ({d['num_blocks']} blocks of 128)",
+        "B": d["B"], "S1": d["S1"], "n_heads": d["n_heads"], "head_dim": d["head_dim"], "topk": d["topk"],
+        "l2": "flushed between timed calls by a 256 MiB write (outside the per-call events)",
+        "launch": "a bounded GPU spin precedes each timed call, so its events time the device, not the host launch",
+        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+    }
+
+
+def indexer_subset(inp, nb):
+    """The first nb sequences of an indexer workload (same cache)."""
+    d = dict(inp["dims"])
+    S1 = d["S1"]
+    d["B"] = nb
+    return dict(inp, dims=d, q=inp["q"][:nb * S1], w=inp["w"][:nb * S1], block_table=inp["block_table"][:nb],
+                act_seqs=inp["act_seqs"][:nb])
+
+
+def time_indexer_oracle(inp, target_s: float):
+    """The oracle (scores, then selection), as it stands, on a bounded sample of
+    sequences; returns (us per full call, cores, sample description)."""
+    import oracle
+    oracle.build()
+    d = inp["dims"]
+    B, S1 = d["B"], d["S1"]
+    cores = oracle.max_threads()
+
+    def run(sub):
+        sc, _ = oracle.indexer_scores(sub)
+        oracle.indexer_select(sc, sub["act_seqs"], S1, d["topk"])
+
+    wave = max(1, min(B, -(-cores // S1)))          # one token per thread
+    t0 = time.perf_counter()
+    run(indexer_subset(inp, wave))
+    t_wave = max(time.perf_counter() - t0, 1e-6)
+    full_est = t_wave * math.ceil(B / wave)
+    if full_est <= target_s:
+        reps = max(1, int(round(target_s / full_est)))
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            run(inp)
+        dt = time.perf_counter() - t0
+        return dt / reps * 1e6, cores, f"all {B} sequences, {reps} oracle calls ({dt:.2f} s)"
+    n = int(min(B, max(wave, round(target_s / t_wave) * wave)))
+    t0 = time.perf_counter()
+    run(indexer_subset(inp, n))
+    dt = time.perf_counter() - t0
+    return dt / n * B * 1e6, cores, f"first {n} of {B} sequences in one oracle call ({dt:.2f} s), scaled to all {B}"
+
+
+def main_indexer(args, world, rank, local_rank):
+    import torch
+    import torch.distributed as dist
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    import mla_sparse_top_gb300 as mla
+    from mla_sparse_top_gb300 import build
+    build.build()
+    mla.load_library()
+
+    inp = workloads.INDEXER_NAMED[args.workload](seed=rank_seed(args.workload, rank))
+    d = inp["dims"]
+    counts = indexer_counts(inp)
+    dev = workloads.indexer_to_device(inp)
+    dims = mla.indexer_dims_from_workload(d)
+    scores = torch.empty(mla.mla_indexer_workspace_bytes(dims) // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def launch_scores():
+        mla.mla_indexer_scores(dev["q"], dev["w"], dev["k_cache"], dev["block_table"], dev["act_seqs"], scores,
+                               dims=dims, stream=stream)
+
+    def launch_select():
+        mla.mla_indexer_select(scores, dev["act_seqs"], dev["topk_idx"], dims=dims, stream=stream)
+
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    for i in range(max(3, args.warmup)):
+        flush.fill_(float(i))
+        launch_scores()
+        launch_select()
+    torch.cuda.synchronize()
+    if mla.indexer_device_status(clear=True):
+        raise RuntimeError("indexer device status reported an error during warm-up")
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.15)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.mark_on()
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        spin_gpu()
+        ev[i][0].record(stream)
+        launch_scores()
+        ev[i][1].record(stream)
+        launch_select()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    clocks.mark_off()
+    if world > 1:
+        dist.barrier()
+    t_scores = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]) * 1000.0)
+    t_select = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]) * 1000.0)
+    t_step = float(np.mean([e[0].elapsed_time(e[2]) for e in ev]) * 1000.0)
+    status = mla.indexer_device_status(clear=True)
+
+    # end to end through the public call with pinned host buffers (the key cache stays resident)
+    host_in = {k: dev[k].cpu().pin_memory() for k in ("q", "w", "block_table", "act_seqs")}
+    host_out = dev["topk_idx"].cpu().pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+    e2e_steps = max(5, min(args.steps, 50))
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    for i in range(e2e_steps + 2):
+        flush.fill_(float(i))
+        k = i - 2
+        if k >= 0:
+            e_s[k].record(stream)
+        for name, t in host_in.items():
+            dev[name].copy_(t, non_blocking=True)
+        mla.mla_indexer_topk(dev["q"], dev["w"], dev["k_cache"], dev["block_table"], dev["act_seqs"],
+                             dev["topk_idx"], scores, dims=dims, stream=stream)
+        host_out.copy_(dev["topk_idx"], non_blocking=True)
+        if k >= 0:
+            e_e[k].record(stream)
+    torch.cuda.synchronize()
+    e2e_us = float(np.mean([a.elapsed_time(b) for a, b in zip(e_s, e_e)]) * 1000.0)
+    clock_summary = clocks.stop()
+    t_step, t_scores, t_select, e2e_us = reduce_max_over_ranks([t_step, t_scores, t_select, e2e_us], device="cuda")
+
+    if rank == 0:
+        hbm_gbs, bf16_tf, peak_src = measured_peaks()
+        per_kernel = {"idx_scores_kernel": t_scores, "idx_topk_kernel": t_select}
+        dom = max(per_kernel, key=per_kernel.get)
+        achieved = counts[dom]["bytes"] / (per_kernel[dom] * 1e-6) / 1e9
+        line = {
+            "metric": INDEXER_METRIC,
+            "value": round(t_step, 3),
+            "unit": UNIT,
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(t_step / 1000.0, 6),
+            "higher_is_better": False,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic",
+            "config": indexer_config(args.workload, d, world),
+            "kernels_us": {k: round(v, 3) for k, v in per_kernel.items()},
+            "roofline": {
+                "bound": "hbm",
+                "achieved": round(achieved, 1),
+                "peak": hbm_gbs,
+                "unit": "GB/s",
+                "frac": round(achieved / hbm_gbs, 4),
+                "traffic": ncu_traffic(args.workload, dom, INDEXER_SOURCE),
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback",
+                "algorithmic_bytes_per_launch": counts[dom]["bytes"],
+                "kernel": dom,
+            },
+            "tensor": {"kernel": "idx_scores_kernel",
+                       "achieved_tflops": round(counts["idx_scores_kernel"]["flops"] / (t_scores * 1e-6) / 1e12, 2),
+                       "peak_tflops": bf16_tf, "flops_per_launch": counts["idx_scores_kernel"]["flops"]},
+            "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": int(d2h)},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clock_summary,
+            "device_status": status,
+        }
+        if not args.no_cpu_baseline:
+            cus, cores, sample = time_indexer_oracle(inp, args.cpu_seconds)
+            line["cpu_baseline"] = {"value": round(cus, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+                                    "sample": sample}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference_indexer(args, world, rank):
+    """The reference arm for an indexer workload: the oracle's scores and
+    selection, as they stand, on the host cores."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    inp = workloads.INDEXER_NAMED[args.workload]()
+    d = inp["dims"]
+    B, S1 = d["B"], d["S1"]
+    cores = oracle.max_threads()
+    per_step = max(1, min(B, -(-cores // S1)))
+    if args.warmup > 0:
+        sub = indexer_subset(inp, 1)
+        oracle.indexer_scores(sub)
+    per_call = []
+    for i in range(args.steps):
+        b0 = (i * per_step) % B
+        nb = min(per_step, B - b0)
+        sub = dict(indexer_subset(dict(inp, q=inp["q"][b0 * S1:], w=inp["w"][b0 * S1:],
+                                       block_table=inp["block_table"][b0:], act_seqs=inp["act_seqs"][b0:]), nb))
+        t0 = time.perf_counter()
+        sc, _ = oracle.indexer_scores(sub)
+        oracle.indexer_select(sc, sub["act_seqs"], S1, d["topk"])
+        per_call.append((time.perf_counter() - t0) / nb * B * 1e6)
+    us = float(np.mean(per_call))
+    sample = f"{per_step} of {B} sequences per step, scaled to all {B} sequences"
+    line = {
+        "metric": INDEXER_METRIC, "value": round(us, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(us / 1000.0, 3), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": indexer_config(args.workload, d, world),
+        "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
 
 
 def run_reference(args, world, rank):

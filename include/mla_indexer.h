@@ -65,12 +65,34 @@ size_t mla_indexer_workspace_bytes(const mla_indexer_dims* dims);
  *             scores as fp32 [B*S1, W*128]: entry [t, j] = I[t, j] for
  *             candidate positions j, -inf for positions below act_seqs[b] that
  *             are not candidates, unspecified at and beyond act_seqs[b].
- * Two launches on `stream` (scores, then selection).  MLA_ERR_SHAPE when the
- * workspace is too small.
+ * Two launches on `stream` (mla_indexer_scores into the workspace, then
+ * mla_indexer_select).  MLA_ERR_SHAPE when the workspace is too small.
  */
 mla_status mla_indexer_topk(const mla_indexer_dims* dims, const void* q, const float* w, const void* k_cache,
                             const int32_t* block_table, const int32_t* act_seqs, int32_t* topk_idx,
                             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The two phases of mla_indexer_topk as separate calls (one launch each), for
+ * callers that want the scores themselves or select from scores of their own.
+ *
+ * mla_indexer_scores: the score phase alone.  scores is the fp32 [B*S1, W*128]
+ * buffer of at least mla_indexer_workspace_bytes(dims) bytes, 256-byte
+ * aligned, filled as the workspace of mla_indexer_topk is.
+ */
+mla_status mla_indexer_scores(const mla_indexer_dims* dims, const void* q, const float* w, const void* k_cache,
+                              const int32_t* block_table, const int32_t* act_seqs, float* scores,
+                              size_t scores_bytes, void* stream);
+
+/*
+ * mla_indexer_select: the selection phase alone, on any fp32 scores laid out
+ * as above (row t = b*S1 + s, leading dimension W*128): among positions
+ * j < act_seqs[b], -inf marks a non-candidate and every other value must be
+ * finite; entries at and beyond act_seqs[b] are not read.  dims->q-side
+ * fields (n_heads, head_dim, num_blocks) are checked as for the score phase.
+ */
+mla_status mla_indexer_select(const mla_indexer_dims* dims, const float* scores, const int32_t* act_seqs,
+                              int32_t* topk_idx, void* stream);
 
 /* Description of the last error of an mla_indexer_* call on this thread
  * (empty after a successful call). */

@@ -26,7 +26,8 @@ MLA_DEVICE_TIMEOUT = 0x2
 
 EXPORTED_SYMBOLS = ("mla_sparse_attn_fwd", "mla_sparse_last_error", "mla_sparse_device_status",
                     "mla_sparse_abi_version", "mla_indexer_workspace_bytes", "mla_indexer_topk",
-                    "mla_indexer_device_status", "mla_indexer_last_error")
+                    "mla_indexer_scores", "mla_indexer_select", "mla_indexer_device_status",
+                    "mla_indexer_last_error")
 
 
 class MlaDims(ctypes.Structure):
@@ -70,6 +71,10 @@ def load_library(path: str = LIB_PATH):
     lib.mla_indexer_workspace_bytes.restype = ctypes.c_size_t
     lib.mla_indexer_topk.argtypes = [ctypes.POINTER(IndexerDims)] + [vp] * 7 + [ctypes.c_size_t, vp]
     lib.mla_indexer_topk.restype = ctypes.c_int
+    lib.mla_indexer_scores.argtypes = [ctypes.POINTER(IndexerDims)] + [vp] * 6 + [ctypes.c_size_t, vp]
+    lib.mla_indexer_scores.restype = ctypes.c_int
+    lib.mla_indexer_select.argtypes = [ctypes.POINTER(IndexerDims)] + [vp] * 4
+    lib.mla_indexer_select.restype = ctypes.c_int
     lib.mla_indexer_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int32]
     lib.mla_indexer_device_status.restype = ctypes.c_int
     lib.mla_indexer_last_error.argtypes = []
@@ -177,6 +182,27 @@ def mla_indexer_topk(q, w, k_cache, block_table, act_seqs, topk_idx, workspace, 
     nbytes = workspace.numel() * workspace.element_size()
     st = lib.mla_indexer_topk(ctypes.byref(dims), _ptr(q), _ptr(w), _ptr(k_cache), _ptr(block_table), _ptr(act_seqs),
                               _ptr(topk_idx), _ptr(workspace), ctypes.c_size_t(nbytes), _stream_handle(stream))
+    _check_idx(st)
+    return topk_idx
+
+
+def mla_indexer_scores(q, w, k_cache, block_table, act_seqs, scores, *, dims: IndexerDims, stream=None):
+    """Enqueue the score phase alone (C entry point of the same name); scores is
+    a device tensor of at least mla_indexer_workspace_bytes(dims) bytes."""
+    lib = load_library()
+    nbytes = scores.numel() * scores.element_size()
+    st = lib.mla_indexer_scores(ctypes.byref(dims), _ptr(q), _ptr(w), _ptr(k_cache), _ptr(block_table),
+                                _ptr(act_seqs), _ptr(scores), ctypes.c_size_t(nbytes), _stream_handle(stream))
+    _check_idx(st)
+    return scores
+
+
+def mla_indexer_select(scores, act_seqs, topk_idx, *, dims: IndexerDims, stream=None):
+    """Enqueue the selection phase alone (C entry point of the same name) on
+    fp32 scores [B*S1, W*128]."""
+    lib = load_library()
+    st = lib.mla_indexer_select(ctypes.byref(dims), _ptr(scores), _ptr(act_seqs), _ptr(topk_idx),
+                                _stream_handle(stream))
     _check_idx(st)
     return topk_idx
 

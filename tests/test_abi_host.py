@@ -30,7 +30,8 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     assert {"mla_sparse_attn_fwd", "mla_sparse_last_error", "mla_sparse_device_status",
             "mla_sparse_abi_version", "mla_indexer_topk", "mla_indexer_workspace_bytes",
-            "mla_indexer_device_status", "mla_indexer_last_error"} <= set(names)
+            "mla_indexer_device_status", "mla_indexer_last_error", "mla_indexer_scores",
+            "mla_indexer_select"} <= set(names)
 
 
 def test_library_exports_every_declared_function(lib):
@@ -171,3 +172,35 @@ def test_indexer_argument_errors_are_reported_before_launch(lib, case, expect):
     st = lib.mla_indexer_topk(dims, q, w, k, bt, act, topk, ws, ctypes.c_size_t(ws_bytes), None)
     assert st == expect, (case, st, lib.mla_indexer_last_error())
     assert lib.mla_indexer_last_error()
+
+
+@pytest.mark.parametrize("case,expect", [("null_scores", -1), ("small", -2), ("misaligned", -5), ("heads_24", -4)])
+def test_indexer_score_phase_argument_errors(lib, case, expect):
+    d = _idims()
+    q, w, k, bt, act, sc = [ctypes.c_void_p(0x100000 * (i + 1)) for i in range(6)]
+    nbytes = 2 * 2 * 8 * 128 * 4
+    if case == "null_scores":
+        sc = None
+    elif case == "small":
+        nbytes = 16
+    elif case == "misaligned":
+        sc = ctypes.c_void_p(0x100040)
+    elif case == "heads_24":
+        d.n_heads = 24
+    st = lib.mla_indexer_scores(ctypes.byref(d), q, w, k, bt, act, sc, ctypes.c_size_t(nbytes), None)
+    assert st == expect, (case, st, lib.mla_indexer_last_error())
+
+
+@pytest.mark.parametrize("case,expect", [("null_out", -1), ("misaligned", -5), ("topk_zero", -2)])
+def test_indexer_select_phase_argument_errors(lib, case, expect):
+    d = _idims()
+    sc, act, out = [ctypes.c_void_p(0x100000 * (i + 1)) for i in range(3)]
+    if case == "null_out":
+        out = None
+    elif case == "misaligned":
+        sc = ctypes.c_void_p(0x100002)
+    elif case == "topk_zero":
+        d.topk = 0
+    st = lib.mla_indexer_select(ctypes.byref(d), sc, act, out, None)
+    assert st == expect, (case, st, lib.mla_indexer_last_error())
+

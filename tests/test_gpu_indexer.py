@@ -157,3 +157,76 @@ def test_full_size_decode_sampled_tokens():
     inp = workloads.indexer_decode()
     idx, sc, st = run_indexer(inp)
     check(inp, idx, sc, tokens=[0, 1, 63, 64, 126, 127], status=st)
+
+
+def test_split_phases_equal_the_combined_call():
+    import mla_sparse_top_gb300 as mla
+    inp = workloads.make_indexer_inputs(B=3, S1=2, act_seqs=[5000, 300, 2049], topk=1024, seed=34)
+    idx, sc, _ = run_indexer(inp)
+    d = inp["dims"]
+    dev = workloads.indexer_to_device(inp)
+    dims = mla.indexer_dims_from_workload(d)
+    scores = torch.empty(mla.mla_indexer_workspace_bytes(dims) // 4, dtype=torch.float32, device="cuda")
+    mla.mla_indexer_scores(dev["q"], dev["w"], dev["k_cache"], dev["block_table"], dev["act_seqs"], scores, dims=dims)
+    mla.mla_indexer_select(scores, dev["act_seqs"], dev["topk_idx"], dims=dims)
+    assert mla.indexer_device_status(clear=True) == 0
+    np.testing.assert_array_equal(dev["topk_idx"].cpu().numpy(), idx)
+    T, ld = d["B"] * d["S1"], d["max_blocks_per_seq"] * 128
+    for t in range(T):
+        n = int(inp["act_seqs"][t // 2])
+        np.testing.assert_array_equal(scores.view(T, ld)[t, :n].cpu().numpy(), sc[t, :n])
+
+
+@pytest.mark.parametrize("kind", ["coarse_ties", "signed_zeros", "sparse_candidates", "all_equal", "extremes"])
+def test_selection_phase_on_given_scores(kind):
+    """The selection kernel alone on fp32 scores built here, against the
+    oracle's selection rule on the same fp32 values."""
+    import mla_sparse_top_gb300 as mla
+    rng = np.random.default_rng(40)
+    B, S1, W, topk = 4, 2, 40, 700
+    ld = W * 128
+    act = np.array([ld, 5000, 699, 1], dtype=np.int32)
+    T = B * S1
+    if kind == "coarse_ties":
+        sc = rng.integers(-20, 20, size=(T, ld)).astype(np.float32)            # many exact ties
+    elif kind == "signed_zeros":
+        sc = np.where(rng.random((T, ld)) < 0.5, np.float32(0.0), np.float32(-0.0)).astype(np.float32)
+        sc[:, ::7] = 1.0
+    elif kind == "sparse_candidates":
+        sc = rng.standard_normal((T, ld)).astype(np.float32)
+        sc[rng.random((T, ld)) < 0.9] = -np.inf                                 # ~10% candidates
+    elif kind == "all_equal":
+        sc = np.full((T, ld), 3.5, dtype=np.float32)
+    else:
+        sc = rng.choice(np.array([np.finfo(np.float32).max, -np.finfo(np.float32).max, np.finfo(np.float32).tiny,
+                                  -np.finfo(np.float32).tiny, 1e-45, -1e-45, 0.0, 1.0], dtype=np.float32),
+                        size=(T, ld))
+    sc = np.ascontiguousarray(sc, dtype=np.float32)
+    d = dict(B=B, S1=S1, n_heads=64, head_dim=128, block_size=128, num_blocks=W, max_blocks_per_seq=W, topk=topk)
+    dims = mla.indexer_dims_from_workload(d)
+    dev_sc = torch.from_numpy(sc).cuda()
+    dev_act = torch.from_numpy(act).cuda()
+    out = torch.full((T, topk), -7, dtype=torch.int32, device="cuda")
+    mla.mla_indexer_select(dev_sc, dev_act, out, dims=dims)
+    assert mla.indexer_device_status(clear=True) == 0
+    np.testing.assert_array_equal(out.cpu().numpy(), oracle.indexer_select(sc, act, S1, topk))
+
+
+@pytest.mark.parametrize("kind", ["gaussian", "coarse_ties"])
+def test_selection_phase_on_rows_longer_than_one_round(kind):
+    """Rows of more than 8192 positions: the later positions are re-read from
+    the scores on every pass."""
+    import mla_sparse_top_gb300 as mla
+    rng = np.random.default_rng(41)
+    B, S1, W, topk = 4, 1, 160, 2048
+    ld = W * 128
+    act = np.array([ld, 9000, 8193, 8192], dtype=np.int32)
+    sc = rng.standard_normal((B, ld)).astype(np.float32)
+    if kind == "coarse_ties":
+        sc = np.round(sc * 4).astype(np.float32)
+    d = dict(B=B, S1=S1, n_heads=64, head_dim=128, block_size=128, num_blocks=W, max_blocks_per_seq=W, topk=topk)
+    dims = mla.indexer_dims_from_workload(d)
+    out = torch.full((B, topk), -7, dtype=torch.int32, device="cuda")
+    mla.mla_indexer_select(torch.from_numpy(sc).cuda(), torch.from_numpy(act).cuda(), out, dims=dims)
+    assert mla.indexer_device_status(clear=True) == 0
+    np.testing.assert_array_equal(out.cpu().numpy(), oracle.indexer_select(sc, act, S1, topk))

@@ -94,6 +94,32 @@ mla_status mla_indexer_scores(const mla_indexer_dims* dims, const void* q, const
 mla_status mla_indexer_select(const mla_indexer_dims* dims, const float* scores, const int32_t* act_seqs,
                               int32_t* topk_idx, void* stream);
 
+/*
+ * mla_indexer_topk_noalloc: mla_indexer_topk without a workspace argument.
+ * No counterpart in the method as described ("CANN DeepSeek Indexer
+ * attention"); it serves callers that cannot allocate device memory at call
+ * time, such as a host program that sizes all its device memory once at
+ * start-up, where a later cudaMalloc could fail or wait for the whole device.
+ *
+ * The scores go to a scratch array inside the library's device image (8 MiB,
+ * created by the CUDA runtime with the module): the call allocates nothing.
+ *   limit       B * S1 * max_blocks_per_seq * 128 <= 2,097,152 scores; larger
+ *               dims return MLA_ERR_SHAPE before any launch, with a message.
+ *   races       one scratch per device and process: calls that overlap in time
+ *               (on other streams or from other host threads) overwrite each
+ *               other's scores.  Serialise them, or use mla_indexer_topk.
+ *   first call  the first call on each device looks the scratch address up
+ *               (cudaGetSymbolAddress) and keeps it; make that first call
+ *               before any stream capture begins.
+ *   zeroing     none is needed: every score the selection reads is written
+ *               by the score phase of the same call.
+ * Arguments, outputs, launches and errors are otherwise those of
+ * mla_indexer_topk.
+ */
+mla_status mla_indexer_topk_noalloc(const mla_indexer_dims* dims, const void* q, const float* w,
+                                    const void* k_cache, const int32_t* block_table, const int32_t* act_seqs,
+                                    int32_t* topk_idx, void* stream);
+
 /* Description of the last error of an mla_indexer_* call on this thread
  * (empty after a successful call). */
 const char* mla_indexer_last_error(void);

@@ -8,10 +8,11 @@ through a thin ctypes binding with the same entry-point names.
 from .binding import (MLA_DEVICE_BAD_BLOCK, MLA_DEVICE_TIMEOUT, MLA_KV_BF16, MLA_KV_INT8, MLA_MODE_DECODE,
                       MLA_MODE_PREFILL, IndexerDims, MlaDims, MlaError, abi_version, device_status, dims_from_workload,
                       indexer_device_status, indexer_dims_from_workload, load_library, mla_indexer_scores,
-                      mla_indexer_select, mla_indexer_topk, mla_indexer_workspace_bytes, mla_sparse_attn_fwd)
+                      mla_indexer_select, mla_indexer_topk, mla_indexer_topk_noalloc, mla_indexer_workspace_bytes,
+                      mla_sparse_attn_fwd)
 
 __all__ = ["mla_sparse_attn_fwd", "device_status", "abi_version", "load_library", "MlaDims", "MlaError", "dims_from_workload",
-           "mla_indexer_topk", "mla_indexer_scores", "mla_indexer_select", "mla_indexer_workspace_bytes", "indexer_device_status", "indexer_dims_from_workload",
+           "mla_indexer_topk", "mla_indexer_topk_noalloc", "mla_indexer_scores", "mla_indexer_select", "mla_indexer_workspace_bytes", "indexer_device_status", "indexer_dims_from_workload",
            "IndexerDims",
            "MLA_MODE_DECODE", "MLA_MODE_PREFILL", "MLA_KV_BF16", "MLA_KV_INT8", "MLA_DEVICE_BAD_BLOCK",
            "MLA_DEVICE_TIMEOUT"]

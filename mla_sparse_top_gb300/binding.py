@@ -27,7 +27,7 @@ MLA_DEVICE_TIMEOUT = 0x2
 EXPORTED_SYMBOLS = ("mla_sparse_attn_fwd", "mla_sparse_last_error", "mla_sparse_device_status",
                     "mla_sparse_abi_version", "mla_indexer_workspace_bytes", "mla_indexer_topk",
                     "mla_indexer_scores", "mla_indexer_select", "mla_indexer_device_status",
-                    "mla_indexer_last_error")
+                    "mla_indexer_last_error", "mla_indexer_topk_noalloc")
 
 
 class MlaDims(ctypes.Structure):
@@ -75,6 +75,8 @@ def load_library(path: str = LIB_PATH):
     lib.mla_indexer_scores.restype = ctypes.c_int
     lib.mla_indexer_select.argtypes = [ctypes.POINTER(IndexerDims)] + [vp] * 4
     lib.mla_indexer_select.restype = ctypes.c_int
+    lib.mla_indexer_topk_noalloc.argtypes = [ctypes.POINTER(IndexerDims)] + [vp] * 7
+    lib.mla_indexer_topk_noalloc.restype = ctypes.c_int
     lib.mla_indexer_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int32]
     lib.mla_indexer_device_status.restype = ctypes.c_int
     lib.mla_indexer_last_error.argtypes = []
@@ -203,6 +205,18 @@ def mla_indexer_select(scores, act_seqs, topk_idx, *, dims: IndexerDims, stream=
     lib = load_library()
     st = lib.mla_indexer_select(ctypes.byref(dims), _ptr(scores), _ptr(act_seqs), _ptr(topk_idx),
                                 _stream_handle(stream))
+    _check_idx(st)
+    return topk_idx
+
+
+def mla_indexer_topk_noalloc(q, w, k_cache, block_table, act_seqs, topk_idx, *, dims: IndexerDims, stream=None):
+    """Enqueue one call of the C entry point with the same name: the indexer
+    and top-k with the scores in the library's fixed scratch (no workspace,
+    nothing allocated; at most 2,097,152 scores per call, and calls that
+    overlap in time race on the scratch)."""
+    lib = load_library()
+    st = lib.mla_indexer_topk_noalloc(ctypes.byref(dims), _ptr(q), _ptr(w), _ptr(k_cache), _ptr(block_table),
+                                      _ptr(act_seqs), _ptr(topk_idx), _stream_handle(stream))
     _check_idx(st)
     return topk_idx
 

@@ -653,6 +653,14 @@ __global__ void __launch_bounds__(kSelThreads) idx_topk_kernel(const SelectParam
 
 }  // namespace mlaidx
 
+// Scratch of mla_indexer_topk_noalloc: the fp32 scores of one call, in the
+// library's own device image (the CUDA runtime creates it with the module), so
+// that the call itself allocates nothing.  Its size is the call's limit:
+// B * S1 * max_blocks_per_seq * 128 scores at most.  One array per device and
+// process: calls that overlap in time (other streams, other host threads)
+// share it and race.
+constexpr size_t kNoAllocScratchFloats = size_t{2} << 20;  // 2 Mi fp32 = 8 MiB
+static __device__ __align__(256) float g_idx_noalloc_scratch[kNoAllocScratchFloats];
 
 // ==================================================================== C ABI
 namespace {
@@ -674,6 +682,9 @@ cudaError_t g_encode_err = cudaSuccess;
 
 constexpr int kMaxDevices = 64;
 std::once_flag g_attr_once[kMaxDevices];
+std::once_flag g_scratch_once[kMaxDevices];
+cudaError_t g_scratch_err[kMaxDevices];
+float* g_scratch_ptr[kMaxDevices];
 cudaError_t g_attr_err[kMaxDevices];
 int g_sm_count[kMaxDevices];
 
@@ -866,6 +877,49 @@ mla_status mla_indexer_topk(const mla_indexer_dims* dims, const void* q, const f
   st = launch_scores(*dims, dev, q, w, k_cache, block_table, act_seqs, scores, s);
   if (st != MLA_OK) return st;
   return launch_select(*dims, scores, act_seqs, topk_idx, s);
+}
+
+// For callers that cannot allocate device memory at call time, e.g. a host
+// program that sizes all its device memory once at start-up, where a later
+// cudaMalloc could fail or wait for the whole device.  Same work as
+// mla_indexer_topk; the scores go to g_idx_noalloc_scratch instead of a
+// caller workspace.  The first call on a device looks the array's address up
+// (cudaGetSymbolAddress) and keeps it; nothing else is set up.
+mla_status mla_indexer_topk_noalloc(const mla_indexer_dims* dims, const void* q, const float* w, const void* k_cache,
+                                    const int32_t* block_table, const int32_t* act_seqs, int32_t* topk_idx,
+                                    void* stream) {
+  g_idx_error[0] = '\0';
+  const mla_status ds = check_dims(dims);
+  if (ds != MLA_OK) return ds;
+  const size_t need = workspace_bytes(*dims);
+  if (need > sizeof(float) * kNoAllocScratchFloats)
+    return idx_fail(MLA_ERR_SHAPE,
+                    "B * S1 * max_blocks_per_seq * 128 = %zu scores exceed the no-allocation scratch of %zu scores; "
+                    "use mla_indexer_topk with a workspace",
+                    need / sizeof(float), kNoAllocScratchFloats);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return idx_fail(MLA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return idx_fail(MLA_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
+  std::call_once(g_scratch_once[dev], [dev] {
+    void* ptr = nullptr;
+    g_scratch_err[dev] = cudaGetSymbolAddress(&ptr, g_idx_noalloc_scratch);
+    g_scratch_ptr[dev] = static_cast<float*>(ptr);
+  });
+  if (g_scratch_err[dev] != cudaSuccess)
+    return idx_fail(MLA_ERR_CUDA, "cudaGetSymbolAddress of the scratch: %s", cudaGetErrorString(g_scratch_err[dev]));
+  float* scratch = g_scratch_ptr[dev];
+  // Nothing in the scratch has to start at zero: the score phase writes every
+  // position below act_seqs[b] before the selection phase of the same call
+  // reads it, and neither reads beyond.
+  int dev2 = 0;
+  mla_status st = check_score_args(dims, q, w, k_cache, block_table, act_seqs, scratch, need, &dev2);
+  if (st == MLA_OK) st = check_select_args(dims, scratch, act_seqs, topk_idx);
+  if (st != MLA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = launch_scores(*dims, dev2, q, w, k_cache, block_table, act_seqs, scratch, s);
+  if (st != MLA_OK) return st;
+  return launch_select(*dims, scratch, act_seqs, topk_idx, s);
 }
 
 mla_status mla_indexer_device_status(void* stream, uint32_t* flags, int32_t clear) {

@@ -31,7 +31,7 @@ def test_header_declares_the_entry_points():
     assert {"mla_sparse_attn_fwd", "mla_sparse_last_error", "mla_sparse_device_status",
             "mla_sparse_abi_version", "mla_indexer_topk", "mla_indexer_workspace_bytes",
             "mla_indexer_device_status", "mla_indexer_last_error", "mla_indexer_scores",
-            "mla_indexer_select"} <= set(names)
+            "mla_indexer_select", "mla_indexer_topk_noalloc"} <= set(names)
 
 
 def test_library_exports_every_declared_function(lib):
@@ -204,3 +204,11 @@ def test_indexer_select_phase_argument_errors(lib, case, expect):
     st = lib.mla_indexer_select(ctypes.byref(d), sc, act, out, None)
     assert st == expect, (case, st, lib.mla_indexer_last_error())
 
+
+def test_indexer_noalloc_rejects_oversize_before_any_cuda_call(lib):
+    d = _idims(B=64, S1=2, max_blocks_per_seq=129)  # 64 * 2 * 129 * 128 scores > 2 Mi
+    p = [ctypes.c_void_p(0x100000 * (i + 1)) for i in range(7)]
+    st = lib.mla_indexer_topk_noalloc(ctypes.byref(d), *p, None)
+    assert st == -2
+    msg = lib.mla_indexer_last_error().decode()
+    assert "exceed" in msg and "mla_indexer_topk" in msg

@@ -509,18 +509,27 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
     // Q latent, dims [128 half, 128 half + 128) of the CTA's 256: the lower half
     // goes to TMEM, the upper half to shared memory (128-byte swizzled rows of
     // 64 dims, head h at row h of chunk (d - 128) / 64)
+    // All loads are issued before the first store: a shared-memory or TMEM store
+    // (inline asm that may touch memory) would otherwise hold back every later
+    // load behind the previous one's full latency.
     const uint8_t* qn = reinterpret_cast<const uint8_t*>(p.q_nope) + (qrow * 512 + c.crank * 256 + half * 128) * 2;
+    // Q rope: this CTA's 32 dims [32 crank, 32 crank + 32), units 2 half, 2 half + 1
+    const uint8_t* qr = reinterpret_cast<const uint8_t*>(p.q_rope) + (qrow * 64 + c.crank * 32 + half * 16) * 2;
+    uint4 qv[16], rv[2];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) qv[u] = live ? ldg16(qn + u * 16) : zero;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) rv[u] = live ? ldg16(qr + u * 16) : zero;
     if (half == 0) {
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         uint32_t w[32];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const uint4 v = live ? ldg16(qn + (ch * 8 + u) * 16) : zero;
-          w[4 * u + 0] = v.x;
-          w[4 * u + 1] = v.y;
-          w[4 * u + 2] = v.z;
-          w[4 * u + 3] = v.w;
+          w[4 * u + 0] = qv[8 * ch + u].x;
+          w[4 * u + 1] = qv[8 * ch + u].y;
+          w[4 * u + 2] = qv[8 * ch + u].z;
+          w[4 * u + 3] = qv[8 * ch + u].w;
         }
         tmem_st_32x32b_x32(tQ + 32 * ch, w);
       }
@@ -529,16 +538,10 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
       for (int ch = 0; ch < 2; ++ch)
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-          sts16(c.sbase + kOffQHalf + ch * (kQHalfBytes / 2) + h * 128 + ((u ^ (h & 7)) << 4),
-                live ? ldg16(qn + (ch * 8 + u) * 16) : zero);
+          sts16(c.sbase + kOffQHalf + ch * (kQHalfBytes / 2) + h * 128 + ((u ^ (h & 7)) << 4), qv[8 * ch + u]);
     }
-    // Q rope: this CTA's 32 dims [32 crank, 32 crank + 32), units 2 half, 2 half + 1
-    const uint8_t* qr = reinterpret_cast<const uint8_t*>(p.q_rope) + (qrow * 64 + c.crank * 32 + half * 16) * 2;
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const uint4 v = live ? ldg16(qr + u * 16) : zero;
-      sts16(c.sbase + kOffQRope + rope_unit(h, 2 * half + u), v);
-    }
+    for (int u = 0; u < 2; ++u) sts16(c.sbase + kOffQRope + rope_unit(h, 2 * half + u), rv[u]);
     fence_proxy_async_smem();
     tmem_wait_st();
     tc_fence_before();

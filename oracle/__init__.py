@@ -1,10 +1,11 @@
-"""TEST INFRASTRUCTURE ONLY: the fp64 CPU oracle for sparse MLA attention and
-for the Lightning Indexer's top-k selection.
+"""TEST INFRASTRUCTURE ONLY: the fp64 CPU oracle for sparse MLA attention, for
+the Lightning Indexer's top-k selection and for the paged cache writer.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
 leg may import this package.  The CUDA product path never imports it and the
-two share no code.  The arithmetic lives in ``mla_oracle.c`` and
-``indexer_oracle.c`` (see their headers for the passages they follow); this
+two share no code.  The arithmetic lives in ``mla_oracle.c``,
+``indexer_oracle.c`` and ``cache_oracle.c`` (see their headers for the passages
+they follow); this
 module only compiles them and marshals numpy arrays through ctypes.
 """
 from __future__ import annotations
@@ -16,7 +17,8 @@ import subprocess
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRCS = [os.path.join(_HERE, "mla_oracle.c"), os.path.join(_HERE, "indexer_oracle.c")]
+_SRCS = [os.path.join(_HERE, "mla_oracle.c"), os.path.join(_HERE, "indexer_oracle.c"),
+         os.path.join(_HERE, "cache_oracle.c")]
 _LIB_PATH = os.path.join(_HERE, "libmla_oracle.so")
 _lib = None
 
@@ -48,6 +50,8 @@ def _load():
         lib.idx_oracle_scores.restype = I
         lib.idx_oracle_select.argtypes = [I, I, P, I, P, I, P]
         lib.idx_oracle_select.restype = I
+        lib.cache_oracle_write.argtypes = [I, I, ctypes.c_int64, P, P, P, P, P, P, ctypes.POINTER(ctypes.c_int64)]
+        lib.cache_oracle_write.restype = I
         _lib = lib
     return _lib
 
@@ -146,3 +150,24 @@ def indexer_select(scores, act_seqs, S1: int, topk: int):
     if rc != 0:
         raise ValueError(f"idx_oracle_select rejected the arguments ({rc})")
     return out
+
+
+def cache_write(k_nope, k_rope, cache_index, kv_nope, kv_rope, kv_scales=None):
+    """Write rows into copies of the given cache arrays (numpy): k_nope (T, 512)
+    and k_rope (T, 64) as bf16 bits (uint16), cache_index (T,) int64 flat rows;
+    kv_nope (rows, 512) uint16 (bf16) or int8 (then kv_scales (rows, 4) fp32),
+    kv_rope (rows, 64) uint16.  Returns (kv_nope, kv_rope, kv_scales, skipped_bad)."""
+    lib = _load()
+    kv_int8 = kv_nope.dtype == np.int8
+    kn = np.array(kv_nope, copy=True, order="C")
+    kr = np.array(kv_rope, dtype=np.uint16, copy=True, order="C")
+    ks = np.array(kv_scales, dtype=np.float32, copy=True, order="C") if kv_int8 else None
+    idx = np.ascontiguousarray(cache_index, dtype=np.int64)
+    bad = ctypes.c_int64(0)
+    rc = lib.cache_oracle_write(int(idx.shape[0]), int(kv_int8), int(kn.shape[0]),
+                                _ptr(np.ascontiguousarray(k_nope, dtype=np.uint16)),
+                                _ptr(np.ascontiguousarray(k_rope, dtype=np.uint16)), _ptr(idx), _ptr(kn), _ptr(kr),
+                                _ptr(ks), ctypes.byref(bad))
+    if rc != 0:
+        raise ValueError(f"cache_oracle_write rejected the arguments ({rc})")
+    return kn, kr, ks, int(bad.value)

@@ -10,6 +10,8 @@ N(0,1) data).  One step = one call of the fused kernel over the whole batch.
 ``--workload indexer_decode`` (or another indexer workload) times the
 Lightning Indexer + top-k instead: B=64 S1=2, 64 heads x 128 dims, 8192 keys
 per sequence, top-2048; one step = the score kernel then the selection kernel.
+``--workload cache_write_decode`` / ``cache_write_prefill`` time the paged
+cache writer (128 / 4096 new rows quantised into an INT8 cache of 4096 blocks).
 
 Prints one JSON line (rank 0).  ``value`` is microseconds per call (the
 device-timed kernel, CUDA events on the launching stream, L2 flushed by a
@@ -52,7 +54,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mtp_decode",
-                    choices=sorted(workloads.NAMED) + sorted(workloads.INDEXER_NAMED))
+                    choices=sorted(workloads.NAMED) + sorted(workloads.INDEXER_NAMED)
+                    + sorted(workloads.CACHE_WRITE_NAMED))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
     return ap.parse_args()
@@ -124,7 +127,8 @@ def ncu_traffic(workload, kernel=KERNEL_NAME, source=KERNEL_SOURCE):
 
 
 SEEDS = {"tiny_decode": 0, "mtp_decode": 1, "int8_decode": 2, "varlen_decode": 3, "prefill": 4,
-         "indexer_decode": 5, "indexer_tiny": 6, "indexer_varlen": 7}
+         "indexer_decode": 5, "indexer_tiny": 6, "indexer_varlen": 7, "cache_write_decode": 8,
+         "cache_write_prefill": 9}
 
 
 def rank_seed(workload: str, rank: int) -> int:
@@ -273,9 +277,13 @@ def main():
     if args.impl == "reference":
         if args.workload in workloads.INDEXER_NAMED:
             return run_reference_indexer(args, world, rank)
+        if args.workload in workloads.CACHE_WRITE_NAMED:
+            return run_reference_cache_write(args, world, rank)
         return run_reference(args, world, rank)
     if args.workload in workloads.INDEXER_NAMED:
         return main_indexer(args, world, rank, local_rank)
+    if args.workload in workloads.CACHE_WRITE_NAMED:
+        return main_cache_write(args, world, rank, local_rank)
 
     import torch
     import torch.distributed as dist
@@ -657,6 +665,166 @@ def run_reference_indexer(args, world, rank):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
         "config": indexer_config(args.workload, d, world),
         "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ paged cache writer
+CACHE_METRIC = "paged MLA cache write µs/call (INT8 quantise + rope copy), % HBM roofline"
+
+
+def cache_write_counts(inp):
+    """Algorithmic bytes: every new row read once (bf16 nope + rope + its index)
+    and written once in the cache's format."""
+    d = inp["dims"]
+    n = int((inp["cache_index"] >= 0).sum())
+    read = n * (1024 + 128) + inp["cache_index"].nbytes
+    write = n * ((512 + 16) if d["kv_int8"] else 1024) + n * 128
+    return read + write
+
+
+def cache_write_config(workload, d, world):
+    return {
+        "workload": f"{workload}: T={d['T']} new rows into a {'INT8' if d['kv_int8'] else 'bf16'} paged cache of "
+                    f"{d['num_blocks']} blocks of 128",
+        "T": d["T"], "kv_dtype": "int8" if d["kv_int8"] else "bf16",
+        "l2": "flushed between timed calls by a 256 MiB write (outside the per-call events)",
+        "launch": "a bounded GPU spin precedes each timed call, so its events time the device, not the host launch",
+        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+    }
+
+
+def time_cache_oracle(inp, target_s: float):
+    import oracle
+    oracle.build()
+    reps, t_used = 0, 0.0
+    while t_used < target_s and reps < 1000:
+        t0 = time.perf_counter()
+        oracle.cache_write(inp["k_nope"], inp["k_rope"], inp["cache_index"], inp["kv_nope"], inp["kv_rope"],
+                           inp["kv_scales"], inplace=True)
+        t_used += time.perf_counter() - t0
+        reps += 1
+    return t_used / reps * 1e6, 1, f"the whole call, {reps} oracle calls ({t_used:.2f} s), writing in place"
+
+
+def main_cache_write(args, world, rank, local_rank):
+    import torch
+    import torch.distributed as dist
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    import mla_sparse_top_gb300 as mla
+    from mla_sparse_top_gb300 import build
+    build.build()
+    mla.load_library()
+    inp = workloads.CACHE_WRITE_NAMED[args.workload](seed=rank_seed(args.workload, rank))
+    d = inp["dims"]
+    dev = workloads.cache_write_to_device(inp)
+    stream = torch.cuda.current_stream()
+
+    def launch():
+        mla.mla_cache_write(dev["k_nope"], dev["k_rope"], dev["cache_index"], dev["kv_nope"], dev["kv_rope"],
+                            dev["kv_scales"], stream=stream)
+
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    for i in range(max(3, args.warmup)):
+        flush.fill_(float(i))
+        launch()
+    torch.cuda.synchronize()
+    if mla.cache_device_status(clear=True):
+        raise RuntimeError("cache writer device status reported an error during warm-up")
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.15)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.mark_on()
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        spin_gpu()
+        starts[i].record(stream)
+        launch()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    clocks.mark_off()
+    if world > 1:
+        dist.barrier()
+    us = float(np.mean([a.elapsed_time(b) for a, b in zip(starts, ends)]) * 1000.0)
+    status = mla.cache_device_status(clear=True)
+    # end to end: the new rows and their indices from pinned host memory, then the call; the
+    # result is the updated device cache, so nothing is read back but the status word
+    host_in = {k: dev[k].cpu().pin_memory() for k in ("k_nope", "k_rope", "cache_index")}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    e2e_steps = max(5, min(args.steps, 50))
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    for i in range(e2e_steps + 2):
+        flush.fill_(float(i))
+        k = i - 2
+        if k >= 0:
+            e_s[k].record(stream)
+        for name, t in host_in.items():
+            dev[name].copy_(t, non_blocking=True)
+        launch()
+        if k >= 0:
+            e_e[k].record(stream)
+    torch.cuda.synchronize()
+    e2e_us = float(np.mean([a.elapsed_time(b) for a, b in zip(e_s, e_e)]) * 1000.0)
+    clock_summary = clocks.stop()
+    us, e2e_us = reduce_max_over_ranks([us, e2e_us], device="cuda")
+    if rank == 0:
+        hbm_gbs, _, peak_src = measured_peaks()
+        nbytes = cache_write_counts(inp)
+        achieved = nbytes / (us * 1e-6) / 1e9
+        line = {
+            "metric": CACHE_METRIC, "value": round(us, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(us / 1000.0, 6), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int8" if d["kv_int8"] else "bf16",
+            "data": "synthetic", "config": cache_write_config(args.workload, d, world),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_gbs, "unit": "GB/s",
+                         "frac": round(achieved / hbm_gbs, 4), "traffic": None,
+                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                         else "fallback",
+                         "algorithmic_bytes_per_launch": nbytes, "kernel": "cache_write_kernel"},
+            "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": args.steps, "clocks": clock_summary, "device_status": status,
+        }
+        if not args.no_cpu_baseline:
+            cus, cores, sample = time_cache_oracle(inp, min(args.cpu_seconds, 5.0))
+            line["cpu_baseline"] = {"value": round(cus, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+                                    "sample": sample}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference_cache_write(args, world, rank):
+    """The reference arm for a cache-write workload: the oracle, as it stands, on one host core."""
+    if rank != 0:
+        return
+    inp = workloads.CACHE_WRITE_NAMED[args.workload]()
+    d = inp["dims"]
+    import oracle
+    oracle.build()
+    per_call = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.cache_write(inp["k_nope"], inp["k_rope"], inp["cache_index"], inp["kv_nope"], inp["kv_rope"],
+                           inp["kv_scales"], inplace=True)
+        per_call.append((time.perf_counter() - t0) * 1e6)
+    us = float(np.mean(per_call))
+    line = {
+        "metric": CACHE_METRIC, "value": round(us, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(us / 1000.0, 3), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "impl": "reference",
+        "config": cache_write_config(args.workload, d, world),
+        "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "the whole call per step, writing in place"},
         "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

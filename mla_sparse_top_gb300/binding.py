@@ -27,7 +27,8 @@ MLA_DEVICE_TIMEOUT = 0x2
 EXPORTED_SYMBOLS = ("mla_sparse_attn_fwd", "mla_sparse_last_error", "mla_sparse_device_status",
                     "mla_sparse_abi_version", "mla_indexer_workspace_bytes", "mla_indexer_topk",
                     "mla_indexer_scores", "mla_indexer_select", "mla_indexer_device_status",
-                    "mla_indexer_last_error", "mla_indexer_topk_noalloc")
+                    "mla_indexer_last_error", "mla_indexer_topk_noalloc", "mla_cache_write",
+                    "mla_cache_last_error", "mla_cache_device_status")
 
 
 class MlaDims(ctypes.Structure):
@@ -77,6 +78,12 @@ def load_library(path: str = LIB_PATH):
     lib.mla_indexer_select.restype = ctypes.c_int
     lib.mla_indexer_topk_noalloc.argtypes = [ctypes.POINTER(IndexerDims)] + [vp] * 7
     lib.mla_indexer_topk_noalloc.restype = ctypes.c_int
+    lib.mla_cache_write.argtypes = [ctypes.c_int32, ctypes.c_int64, ctypes.c_int32] + [vp] * 7
+    lib.mla_cache_write.restype = ctypes.c_int
+    lib.mla_cache_last_error.argtypes = []
+    lib.mla_cache_last_error.restype = ctypes.c_char_p
+    lib.mla_cache_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int32]
+    lib.mla_cache_device_status.restype = ctypes.c_int
     lib.mla_indexer_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int32]
     lib.mla_indexer_device_status.restype = ctypes.c_int
     lib.mla_indexer_last_error.argtypes = []
@@ -227,4 +234,28 @@ def indexer_device_status(clear: bool = True, stream=None) -> int:
     st = lib.mla_indexer_device_status(_stream_handle(stream), ctypes.byref(flags), 1 if clear else 0)
     if st not in (MLA_OK, -7):
         _check_idx(st)
+    return int(flags.value)
+
+
+# ------------------------------------------------------------------ paged cache writer
+def mla_cache_write(k_nope, k_rope, cache_index, kv_nope, kv_rope, kv_scales=None, *, stream=None):
+    """Enqueue one call of the C entry point with the same name: k_nope (T, 512)
+    and k_rope (T, 64) bf16, cache_index (T,) int64 flat rows; kv_nope (rows,
+    512) bf16 or int8 (then kv_scales (rows, 4) fp32) and kv_rope (rows, 64)
+    bf16 are updated in place."""
+    lib = load_library()
+    kv_int8 = 1 if kv_nope.element_size() == 1 else 0
+    st = lib.mla_cache_write(int(cache_index.shape[0]), int(kv_nope.shape[0]), kv_int8, _ptr(k_nope), _ptr(k_rope),
+                             _ptr(cache_index), _ptr(kv_nope), _ptr(kv_rope), _ptr(kv_scales),
+                             _stream_handle(stream))
+    if st != MLA_OK:
+        raise MlaError(st, lib.mla_cache_last_error().decode())
+
+
+def cache_device_status(clear: bool = True, stream=None) -> int:
+    lib = load_library()
+    flags = ctypes.c_uint32(0)
+    st = lib.mla_cache_device_status(_stream_handle(stream), ctypes.byref(flags), 1 if clear else 0)
+    if st not in (MLA_OK, -7):
+        raise MlaError(st, lib.mla_cache_last_error().decode())
     return int(flags.value)

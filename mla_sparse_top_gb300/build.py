@@ -7,12 +7,13 @@ import subprocess
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
-SOURCES = [os.path.join(CSRC, "mla_sparse_fwd.cu"), os.path.join(CSRC, "lightning_indexer.cu")]
+SOURCES = [os.path.join(CSRC, "mla_sparse_fwd.cu"), os.path.join(CSRC, "lightning_indexer.cu"),
+           os.path.join(CSRC, "cache_write.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, "ptx.cuh"), os.path.join(ROOT, "include", "mla_sparse.h"),
-                  os.path.join(ROOT, "include", "mla_indexer.h")]
+                  os.path.join(ROOT, "include", "mla_indexer.h"), os.path.join(ROOT, "include", "mla_cache.h")]
 LIB_PATH = os.path.join(HERE, "libmla_sparse.so")
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
-              "-Xcompiler", "-fPIC", "-shared", "--threads", "2"]
+              "-Xcompiler", "-fPIC", "-shared", "--threads", "3"]
 
 
 def nvcc() -> str:

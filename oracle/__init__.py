@@ -152,16 +152,23 @@ def indexer_select(scores, act_seqs, S1: int, topk: int):
     return out
 
 
-def cache_write(k_nope, k_rope, cache_index, kv_nope, kv_rope, kv_scales=None):
-    """Write rows into copies of the given cache arrays (numpy): k_nope (T, 512)
-    and k_rope (T, 64) as bf16 bits (uint16), cache_index (T,) int64 flat rows;
-    kv_nope (rows, 512) uint16 (bf16) or int8 (then kv_scales (rows, 4) fp32),
-    kv_rope (rows, 64) uint16.  Returns (kv_nope, kv_rope, kv_scales, skipped_bad)."""
+def cache_write(k_nope, k_rope, cache_index, kv_nope, kv_rope, kv_scales=None, inplace=False):
+    """Write rows into copies of the given cache arrays (numpy), or into the
+    arrays themselves with ``inplace`` (they must then be C-contiguous of the
+    right dtypes): k_nope (T, 512) and k_rope (T, 64) as bf16 bits (uint16),
+    cache_index (T,) int64 flat rows; kv_nope (rows, 512) uint16 (bf16) or int8
+    (then kv_scales (rows, 4) fp32), kv_rope (rows, 64) uint16.  Returns
+    (kv_nope, kv_rope, kv_scales, skipped_bad)."""
     lib = _load()
     kv_int8 = kv_nope.dtype == np.int8
-    kn = np.array(kv_nope, copy=True, order="C")
-    kr = np.array(kv_rope, dtype=np.uint16, copy=True, order="C")
-    ks = np.array(kv_scales, dtype=np.float32, copy=True, order="C") if kv_int8 else None
+    if inplace:
+        kn, kr, ks = kv_nope, kv_rope, (kv_scales if kv_int8 else None)
+        assert kn.flags.c_contiguous and kr.flags.c_contiguous and kr.dtype == np.uint16
+        assert ks is None or (ks.flags.c_contiguous and ks.dtype == np.float32)
+    else:
+        kn = np.array(kv_nope, copy=True, order="C")
+        kr = np.array(kv_rope, dtype=np.uint16, copy=True, order="C")
+        ks = np.array(kv_scales, dtype=np.float32, copy=True, order="C") if kv_int8 else None
     idx = np.ascontiguousarray(cache_index, dtype=np.int64)
     bad = ctypes.c_int64(0)
     rc = lib.cache_oracle_write(int(idx.shape[0]), int(kv_int8), int(kn.shape[0]),

@@ -8,7 +8,8 @@ import re
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADERS = [os.path.join(ROOT, "include", "mla_sparse.h"), os.path.join(ROOT, "include", "mla_indexer.h")]
+HEADERS = [os.path.join(ROOT, "include", "mla_sparse.h"), os.path.join(ROOT, "include", "mla_indexer.h"),
+           os.path.join(ROOT, "include", "mla_cache.h")]
 
 
 @pytest.fixture(scope="module")
@@ -22,7 +23,7 @@ def declared_functions():
     names = set()
     for h in HEADERS:
         text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
-        names |= set(re.findall(r"\b(mla_(?:sparse|indexer)_\w+)\s*\(", text))
+        names |= set(re.findall(r"\b(mla_(?:sparse|indexer|cache)_\w+)\s*\(", text))
     return sorted(names)
 
 
@@ -31,7 +32,8 @@ def test_header_declares_the_entry_points():
     assert {"mla_sparse_attn_fwd", "mla_sparse_last_error", "mla_sparse_device_status",
             "mla_sparse_abi_version", "mla_indexer_topk", "mla_indexer_workspace_bytes",
             "mla_indexer_device_status", "mla_indexer_last_error", "mla_indexer_scores",
-            "mla_indexer_select", "mla_indexer_topk_noalloc"} <= set(names)
+            "mla_indexer_select", "mla_indexer_topk_noalloc", "mla_cache_write", "mla_cache_last_error",
+            "mla_cache_device_status"} <= set(names)
 
 
 def test_library_exports_every_declared_function(lib):
@@ -212,3 +214,31 @@ def test_indexer_noalloc_rejects_oversize_before_any_cuda_call(lib):
     assert st == -2
     msg = lib.mla_indexer_last_error().decode()
     assert "exceed" in msg and "mla_indexer_topk" in msg
+
+
+@pytest.mark.parametrize("case,expect", [("negative_T", -2), ("no_rows", -2), ("bad_mode", -2), ("null_src", -1),
+                                         ("int8_no_scales", -1), ("misaligned_cache", -5), ("misaligned_index", -5),
+                                         ("empty", 0)])
+def test_cache_write_argument_errors_are_reported_before_launch(lib, case, expect):
+    T, rows, mode = 4, 256, 1
+    p = [ctypes.c_void_p(0x100000 * (i + 1)) for i in range(6)]  # k_nope k_rope index kv_nope kv_rope kv_scales
+    if case == "negative_T":
+        T = -1
+    elif case == "no_rows":
+        rows = 0
+    elif case == "bad_mode":
+        mode = 2
+    elif case == "null_src":
+        p[0] = None
+    elif case == "int8_no_scales":
+        p[5] = None
+    elif case == "misaligned_cache":
+        p[3] = ctypes.c_void_p(0x100004)
+    elif case == "misaligned_index":
+        p[2] = ctypes.c_void_p(0x100004)
+    elif case == "empty":
+        T = 0
+    st = lib.mla_cache_write(T, ctypes.c_int64(rows), mode, *p, None)
+    assert st == expect, (case, st, lib.mla_cache_last_error())
+    if expect != 0:
+        assert lib.mla_cache_last_error()

@@ -288,3 +288,76 @@ def indexer_to_device(inp: dict, device="cuda") -> dict:
     dev["topk_idx"] = torch.empty((T, d["topk"]), dtype=torch.int32, device=device)
     dev["scores"] = torch.empty((T, d["max_blocks_per_seq"] * d["block_size"]), dtype=torch.float32, device=device)
     return dev
+
+
+# ------------------------------------------------------------------ paged cache writer
+def make_cache_write_inputs(*, T: int, num_blocks: int, kv_int8: bool, seed: int, skip_every: int = 17,
+                            name: str = "custom") -> dict:
+    """New key rows for the paged cache writer and the cache they go into.
+
+    k_nope (T, 512) bf16 ~ N(0, s_t^2) with a per-row s_t ~ U(0.01, 10), plus
+    special rows (a zero group, exact multiples of 2^-3 with a +-127 extreme,
+    half-way ties at scale 1); k_rope (T, 64) bf16 ~ N(0, 1); cache_index:
+    distinct random flat rows, every ``skip_every``-th entry -1.  The existing
+    cache holds random rows (bf16, or INT8 codes with scales)."""
+    g = torch.Generator().manual_seed(int(seed))
+    rows = num_blocks * BLOCK_SIZE
+    assert T <= rows
+    scale_t = torch.empty((T, 1)).uniform_(0.01, 10.0, generator=g)
+    x = torch.randn((T, D_NOPE), generator=g) * scale_t
+    if T >= 3:
+        x[0, 128:256] = 0.0
+        k = torch.randint(-127, 128, (D_NOPE,), generator=g).to(torch.float32)
+        k[5] = 127.0
+        k[133] = -127.0
+        k[261] = 127.0
+        k[389] = -127.0
+        x[1] = k * 2.0 ** -3
+        x[2] = 0.0
+        x[2, 0] = 127.0
+        x[2, 1:9] = torch.tensor([0.5, 1.5, 2.5, -0.5, -1.5, -2.5, 3.5, 126.5])
+    k_nope = _bf16_bits(x)
+    k_rope = _bf16_bits(torch.randn((T, D_ROPE), generator=g))
+    idx = torch.randperm(rows, generator=g)[:T].to(torch.int64).numpy()
+    if skip_every:
+        idx[::skip_every] = -1
+    kv_rope = _bf16_bits(torch.randn((rows, D_ROPE), generator=g))
+    if kv_int8:
+        kv_nope = torch.randint(-127, 128, (rows, D_NOPE), generator=g).to(torch.int8).numpy()
+        kv_scales = torch.empty((rows, 4)).uniform_(0.001, 0.1, generator=g).numpy().astype(np.float32)
+    else:
+        kv_nope = _bf16_bits(torch.randn((rows, D_NOPE), generator=g))
+        kv_scales = None
+    return dict(name=name, k_nope=k_nope, k_rope=k_rope, cache_index=idx, kv_nope=kv_nope, kv_rope=kv_rope,
+                kv_scales=kv_scales, dims=dict(T=T, num_blocks=num_blocks, kv_int8=int(bool(kv_int8))))
+
+
+def cache_write_decode(seed: int = 8) -> dict:
+    """128 new rows (B=64 x S1=2 decode tokens) into an INT8 cache of 4096 blocks."""
+    return make_cache_write_inputs(T=128, num_blocks=4096, kv_int8=True, seed=seed, skip_every=0,
+                                   name="cache_write_decode")
+
+
+def cache_write_prefill(seed: int = 9) -> dict:
+    """4096 new rows (B=4 x 1024 prefill tokens) into an INT8 cache of 4096 blocks."""
+    return make_cache_write_inputs(T=4096, num_blocks=4096, kv_int8=True, seed=seed, skip_every=0,
+                                   name="cache_write_prefill")
+
+
+CACHE_WRITE_NAMED = {
+    "cache_write_decode": cache_write_decode,
+    "cache_write_prefill": cache_write_prefill,
+}
+
+
+def cache_write_to_device(inp: dict, device="cuda") -> dict:
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+    def raw(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+    int8 = inp["dims"]["kv_int8"]
+    return dict(k_nope=bf(inp["k_nope"]), k_rope=bf(inp["k_rope"]), cache_index=raw(inp["cache_index"]),
+                kv_nope=raw(inp["kv_nope"]) if int8 else bf(inp["kv_nope"]), kv_rope=bf(inp["kv_rope"]),
+                kv_scales=raw(inp["kv_scales"]) if int8 else None)

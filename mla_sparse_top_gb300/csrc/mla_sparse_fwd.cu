@@ -118,13 +118,16 @@ constexpr int kBarPvDone = kBarPFull + kRegions;         // [kRegions] P(i).V ac
 constexpr int kBarRecvFull = kBarPvDone + kRegions;      // [2]
 constexpr int kBarPeerFree = kBarRecvFull + 2;           // [2]
 constexpr int kBarPairA = kBarPeerFree + 2;              // [4]
-constexpr int kBarQReady = kBarPairA + 4;
-constexpr int kBarFinal = kBarQReady + 1;
+constexpr int kBarQReady = kBarPairA + 4;   // phase m: Q of the cluster's m-th token is loaded
+constexpr int kBarQFree = kBarQReady + 1;    // phase m: the score MMAs of the m-th token are complete
+constexpr int kBarOFree = kBarQFree + 1;     // phase m: O of the m-th token has been read out
+constexpr int kBarFinal = kBarOFree + 1;
 constexpr int kNumBars = kBarFinal + 1;
 constexpr int kOffTmemSlot = kOffBars + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
 constexpr int kOffZero = kOffAbort + 4;  // a zero the compiler cannot see (dependency anchor)
-constexpr int kSmemBytes = kOffZero + 4;
+constexpr int kOffTotal = kOffZero + 4;  // the cluster's tile count (read where registers are short)
+constexpr int kSmemBytes = kOffTotal + 4;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffStages % 1024 == 0 && kStageBytes % 1024 == 0 && kOffQHalf % 1024 == 0 && kOffQRope % 512 == 0,
               "operand alignment");
@@ -158,6 +161,8 @@ struct Params {
   uint16_t* out;
   float* lse;
   int S1, n_q, topk, num_blocks, mbps, n_tiles;
+  int T;           // query tokens B * S1
+  int n_clusters;  // clusters in the grid; cluster c takes tokens c, c + n_clusters, ...
   float scale_log2;
 };
 
@@ -166,10 +171,15 @@ struct Ctx {
   uint8_t* smem;
   uint32_t tmem;
   uint32_t crank;
-  int t;
+  int cid;    // cluster index
+  int ntok;   // tokens of this cluster
+  int total;  // key tiles of this cluster: ntok * n_tiles, one stream across its tokens
   volatile uint32_t* abort;
   __device__ uint32_t bar(int i) const { return sbase + kOffBars + 8 * i; }
 };
+
+// Token of the m-th tile group of this cluster's stream.
+__device__ __forceinline__ int token_of(const Params& p, const Ctx& c, int m) { return c.cid + m * p.n_clusters; }
 
 __device__ __forceinline__ bool wait_bar(const Ctx& c, int idx, uint32_t parity) {
   return mbar_wait<false>(c.bar(idx), parity, c.abort, kWaitLimitNs);
@@ -187,6 +197,11 @@ __device__ __forceinline__ uint4 ldg16(const void* p) { return __ldg(reinterpret
 __device__ __forceinline__ void sts16(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
+}
+__device__ __forceinline__ int lds_s32(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
 }
 __device__ __forceinline__ float4 lds16f(uint32_t addr) {
   float4 v;
@@ -210,39 +225,56 @@ __device__ __forceinline__ uint32_t xchg_offset(int h, int k) {
 // current one.
 static_assert(kIdxBatch == 4, "two entries per lane per tile, four tiles per pass");
 
-// top-k entries of the pass starting at tile j0 (-1 beyond the list)
-__device__ __forceinline__ void index_load(const Params& p, const int32_t* tk, int j0, int lane, int (&idx)[8]) {
+// Sequence of stream tile jj (jj < c.total).
+__device__ __forceinline__ int seq_of_tile(const Params& p, const Ctx& c, int jj) {
+  return token_of(p, c, jj / p.n_tiles) / p.S1;
+}
+
+// top-k entries of the pass starting at stream tile j0 (-1 beyond the stream
+// or the list)
+__device__ __forceinline__ void index_load(const Params& p, const Ctx& c, int j0, int lane, int (&idx)[8]) {
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const int e = (j0 + (q >> 1)) * kTileKeys + (q & 1) * 32 + lane;
-    idx[q] = (j0 + (q >> 1) < p.n_tiles && e < p.topk) ? __ldg(tk + e) : -1;
+  for (int k = 0; k < kIdxBatch; ++k) {
+    const int jj = j0 + k;
+    const int m = jj / p.n_tiles;
+    const int e0 = (jj - m * p.n_tiles) * kTileKeys + lane;
+    const int32_t* tk = p.topk_idx + static_cast<int64_t>(token_of(p, c, m)) * p.topk;
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+      idx[2 * k + u] = (jj < c.total && e0 + 32 * u < p.topk) ? __ldg(tk + e0 + 32 * u) : -1;
   }
 }
 
-// `idx` holds the entries of this warp's first pass and `act` the token's
-// sequence length, both loaded before the CTA's set-up barrier.
-__device__ void index_role(const Params& p, const Ctx& c, int iw, int lane, int (&idx)[8], int act) {
-  const int b = c.t / p.S1;
-  const int32_t* tk = p.topk_idx + static_cast<int64_t>(c.t) * p.topk;
-  const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.mbps;
+// `idx` holds the entries of this warp's first pass, loaded before the CTA's
+// set-up barrier.  The stream runs through the cluster's tokens in order; a
+// pass may straddle two tokens, so each tile's sequence is found from its
+// position in the stream.
+__device__ void index_role(const Params& p, const Ctx& c, int iw, int lane, int (&idx)[8]) {
   int32_t* rows = reinterpret_cast<int32_t*>(c.smem + kOffRows);
-  // pull this token's top-k row and its sequence's block-table row towards
+  // pull the cluster's top-k rows and their sequences' block-table rows towards
   // L2 up front (one 128-byte line per prefetch; the warps split the lines)
-  for (int e = (iw * 32 + lane) * 32; e < p.topk + 32; e += kIndexWarps * 32 * 32) prefetch_l2(tk + min(e, p.topk - 1));
-  for (int e = (iw * 32 + lane) * 32; e < p.mbps + 32; e += kIndexWarps * 32 * 32) prefetch_l2(bt + min(e, p.mbps - 1));
+  for (int m = 0; m < c.ntok; ++m) {
+    const int t = token_of(p, c, m);
+    const int32_t* tk = p.topk_idx + static_cast<int64_t>(t) * p.topk;
+    const int32_t* bt = p.block_table + static_cast<int64_t>(t / p.S1) * p.mbps;
+    for (int e = (iw * 32 + lane) * 32; e < p.topk + 32; e += kIndexWarps * 32 * 32) prefetch_l2(tk + min(e, p.topk - 1));
+    for (int e = (iw * 32 + lane) * 32; e < p.mbps + 32; e += kIndexWarps * 32 * 32) prefetch_l2(bt + min(e, p.mbps - 1));
+  }
   bool bad = false;
-  for (int j0 = iw * kIdxBatch; j0 < p.n_tiles; j0 += kIndexWarps * kIdxBatch) {
-    const int nb = min(kIdxBatch, p.n_tiles - j0);
+  for (int j0 = iw * kIdxBatch; j0 < c.total; j0 += kIndexWarps * kIdxBatch) {
+    const int nb = min(kIdxBatch, c.total - j0);
     int blk[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       // the table entry is loaded for any index inside the table (without
       // waiting for the length check); entries outside [0, act) are dropped below
       const int slot = idx[q] >> 7;
-      blk[q] = (idx[q] >= 0 && slot < p.mbps) ? __ldg(bt + slot) : -1;
+      blk[q] = (idx[q] >= 0 && slot < p.mbps)
+                   ? __ldg(p.block_table + static_cast<int64_t>(seq_of_tile(p, c, j0 + (q >> 1))) * p.mbps + slot)
+                   : -1;
     }
     int nxt[8];
-    index_load(p, tk, j0 + kIndexWarps * kIdxBatch, lane, nxt);
+    index_load(p, c, j0 + kIndexWarps * kIdxBatch, lane, nxt);
     bool ok = true;
     for (int k = 0; k < nb && ok; ++k) {
       const int j = j0 + k;
@@ -250,14 +282,18 @@ __device__ void index_role(const Params& p, const Ctx& c, int iw, int lane, int 
     }
     if (!ok) break;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      if ((q >> 1) >= nb) continue;
-      const bool in_seq = idx[q] >= 0 && idx[q] < act;
-      const bool valid = in_seq && blk[q] >= 0 && blk[q] < p.num_blocks;
-      if (in_seq && !valid) bad = true;
-      const int row = blk[q] * 128 + (idx[q] & 127);
-
-      rows[((j0 + (q >> 1)) % kIdxSlots) * kTileKeys + (q & 1) * 32 + lane] = valid ? row : -1;
+    for (int k = 0; k < kIdxBatch; ++k) {
+      if (k >= nb) continue;
+      const int act = __ldg(p.act_seqs + seq_of_tile(p, c, j0 + k));
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int q = 2 * k + u;
+        const bool in_seq = idx[q] >= 0 && idx[q] < act;
+        const bool valid = in_seq && blk[q] >= 0 && blk[q] < p.num_blocks;
+        if (in_seq && !valid) bad = true;
+        const int row = blk[q] * 128 + (idx[q] & 127);
+        rows[((j0 + k) % kIdxSlots) * kTileKeys + u * 32 + lane] = valid ? row : -1;
+      }
     }
     for (int k = 0; k < nb; ++k) mbar_arrive(c.bar(kBarIdxFull + ((j0 + k) % kIdxSlots)));
 #pragma unroll
@@ -294,7 +330,7 @@ __device__ void gather_role(const Params& p, const Ctx& c, int gw, int lane) {
   uint8_t* vmask8 = c.smem + kOffVmask;
   const uint8_t* kvr = reinterpret_cast<const uint8_t*>(p.kv_rope) + c.crank * 64 + (lane & 3) * 16;
   const int rk = key0 + (lane >> 2);  // rope: four 16-byte units per key, one per lane
-  for (int j = 0; j < p.n_tiles; ++j) {
+  for (int j = 0; j < c.total; ++j) {
     const int st = j % kStages;
     const int slot = j % kIdxSlots;
     if (!warp_wait(c, kBarEmpty + st, ((j / kStages) & 1) ^ 1)) break;
@@ -396,7 +432,9 @@ __device__ void sender_role(const Params& p, const Ctx& c, int q, int lane) {
   const uint32_t dst = mapa_shared(c.sbase + kOffRecv, peer);
   const uint32_t rbar0 = mapa_shared(c.bar(kBarRecvFull + 0), peer);
   const uint32_t rbar1 = mapa_shared(c.bar(kBarRecvFull + 1), peer);
-  for (int j = 0; j < p.n_tiles; ++j) {
+  // the loop bound comes from shared memory: the two 32-column halves held in
+  // registers leave none to spare for it
+  for (int j = 0; j < lds_s32(c.sbase + kOffTotal); ++j) {
     const int r = j % kRegions;
     if (!warp_wait(c, kBarSFull + r, (j / kRegions) & 1)) break;
     tc_fence_after();
@@ -441,7 +479,7 @@ __device__ __forceinline__ void issue_s(const Ctx& c, int k) {
   umma_commit(c.bar(kBarSFull + k % kRegions));
 }
 
-__device__ __forceinline__ void issue_pv(const Ctx& c, int i) {
+__device__ __forceinline__ void issue_pv(const Ctx& c, int i, bool first_of_token) {
   constexpr uint32_t idesc = make_idesc_f16(128, 256, 1, 0, 1);
   const uint32_t stage = c.sbase + kOffStages + (i % kStages) * kStageBytes;
   const uint32_t aP = c.tmem + kTmemRegion + 64 * (i % kRegions);
@@ -451,7 +489,7 @@ __device__ __forceinline__ void issue_pv(const Ctx& c, int i) {
   for (int s = 0; s < 8; ++s)
     umma_ts(c.tmem + kTmemO, aP + (s < 4 ? 0 : 32) + 8 * (s & 3),
             make_sdesc(stage + (s & 3) * 16 * 128, kChunkBytes, 1024, kSwizzle128B), idesc,
-            (i > 0 || s > 0) ? 1u : 0u);
+            (!first_of_token || s > 0) ? 1u : 0u);
   umma_commit(c.bar(kBarPvDone + i % kRegions));
   umma_commit(c.bar(kBarEmpty + (i % kStages)));
 }
@@ -460,22 +498,45 @@ __device__ __forceinline__ void issue_pv(const Ctx& c, int i) {
 // soon as the softmax has written P(kp), and S(ks) once its key tile has
 // landed and P.V(ks - 3) has released TMEM region ks % 3, so a stage is
 // released as early as the data allows and the softmax of one tile overlaps
-// with the P.V of the previous one.
+// with the P.V of the previous one.  The stream runs through the cluster's
+// tokens: the first S of token m also waits for its Q (QReady phase m), the
+// last S of a token is followed by a commit to QFree (its Q may then be
+// replaced), and the first P.V of token m > 0 waits until O of token m - 1 has
+// been read out (OFree phase m - 1) and starts a fresh accumulator.
 __device__ void mma_role(const Params& p, const Ctx& c) {
-  bool ok = wait_bar(c, kBarQReady, 0);
+  bool ok = true;
   int ks = 0, kp = 0;
+  int s_tok = 0, s_in = 0;  // token ordinal and tile-in-token of ks
+  int p_tok = 0, p_in = 0;  // the same for kp
+  bool s_q = false;         // Q of token s_tok seen ready
   uint64_t t_idle = 0;
   uint32_t spins = 0;
-  while (ok && kp < p.n_tiles) {
+  while (ok && kp < c.total) {
     bool progressed = false;
-    if (kp < ks && mbar_poll(c.bar(kBarPFull + kp % kRegions), (kp / kRegions) & 1)) {
-      issue_pv(c, kp++);
+    if (kp < ks && mbar_poll(c.bar(kBarPFull + kp % kRegions), (kp / kRegions) & 1) &&
+        (p_in != 0 || p_tok == 0 || mbar_poll(c.bar(kBarOFree), (p_tok - 1) & 1))) {
+      issue_pv(c, kp, p_in == 0);
+      ++kp;
+      if (++p_in == p.n_tiles) {
+        p_in = 0;
+        ++p_tok;
+      }
       progressed = true;
     }
-    if (ks < p.n_tiles && mbar_poll(c.bar(kBarFull + ks % kStages), (ks / kStages) & 1) &&
-        (ks < kRegions || mbar_poll(c.bar(kBarPvDone + ks % kRegions), ((ks / kRegions) & 1) ^ 1))) {
-      issue_s(c, ks++);
-      progressed = true;
+    if (ks < c.total) {
+      if (!s_q) s_q = mbar_poll(c.bar(kBarQReady), s_tok & 1);
+      if (s_q && mbar_poll(c.bar(kBarFull + ks % kStages), (ks / kStages) & 1) &&
+          (ks < kRegions || mbar_poll(c.bar(kBarPvDone + ks % kRegions), ((ks / kRegions) & 1) ^ 1))) {
+        issue_s(c, ks);
+        ++ks;
+        if (++s_in == p.n_tiles) {
+          umma_commit(c.bar(kBarQFree));  // the token's score MMAs: its Q may be replaced
+          s_in = 0;
+          ++s_tok;
+          s_q = false;
+        }
+        progressed = true;
+      }
     }
     if (progressed) {
       spins = 0;
@@ -493,22 +554,14 @@ __device__ void mma_role(const Params& p, const Ctx& c) {
 }
 
 // ------------------------------------------------------------------ softmax warps
-__device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) {
-  const int q = warp & 3;          // TMEM lane quadrant
-  const int half = warp >> 2;      // key columns [32 half, 32 half + 32)
-  const int h = q * 32 + lane;     // head
-  const int tid = warp * 32 + lane;
-  const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-  const uint32_t tR = c.tmem + lane_off + kTmemRegion;  // + 64 * (i % kRegions)
-  const uint32_t tO = c.tmem + lane_off + kTmemO + 128 * half;
-  const uint32_t tQ = c.tmem + lane_off + kTmemQ;
-  const bool live = h < p.n_q;
-  const int64_t qrow = static_cast<int64_t>(c.t) * p.n_q + h;
+// Q of token qrow / n_q: latent dims [128 half, 128 half + 128) of the CTA's
+// 256 (the lower half to TMEM, the upper half to shared memory as 128-byte
+// swizzled rows of 64 dims, head h at row h of chunk (d - 128) / 64) and the
+// CTA's rope dims; then QReady.
+__device__ __forceinline__ void load_q(const Params& p, const Ctx& c, int h, int half, bool live, int64_t qrow,
+                                       uint32_t tQ) {
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
   {
-    // Q latent, dims [128 half, 128 half + 128) of the CTA's 256: the lower half
-    // goes to TMEM, the upper half to shared memory (128-byte swizzled rows of
-    // 64 dims, head h at row h of chunk (d - 128) / 64)
     // All loads are issued before the first store: a shared-memory or TMEM store
     // (inline asm that may touch memory) would otherwise hold back every later
     // load behind the previous one's full latency.
@@ -547,6 +600,22 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
     tc_fence_before();
     mbar_arrive(c.bar(kBarQReady));
   }
+}
+
+// The cluster's tokens in order.  Before the epilogue of token m the warps load
+// Q of token m + 1 (once QFree says the score MMAs of token m are complete),
+// so the next token's first score tiles are computed while O of token m is
+// read out; after reading O they arrive on OFree.
+__device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) {
+  const int q = warp & 3;          // TMEM lane quadrant
+  const int half = warp >> 2;      // key columns [32 half, 32 half + 32)
+  const int h = q * 32 + lane;     // head
+  const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+  const uint32_t tR = c.tmem + lane_off + kTmemRegion;  // + 64 * (i % kRegions)
+  const uint32_t tO = c.tmem + lane_off + kTmemO + 128 * half;
+  const uint32_t tQ = c.tmem + lane_off + kTmemQ;
+  const bool live = h < p.n_q;
+  load_q(p, c, h, half, live, static_cast<int64_t>(token_of(p, c, 0)) * p.n_q + h, tQ);
   const uint32_t peer = c.crank ^ 1u;
   const uint32_t dep_zero = *reinterpret_cast<volatile uint32_t*>(c.smem + kOffZero);
   float* pair = reinterpret_cast<float*>(c.smem + kOffPair);
@@ -557,141 +626,160 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
   // score is scaled first and mul = 1
   const bool raw_max = scl > 0.f;
   const float mul = raw_max ? scl : 1.f;
-  float m = -INFINITY, l = 0.f;
-  bool ok = true;
-  for (int i = 0; i < p.n_tiles; ++i) {
-    {
-      // own partial score tile i, read out at once so the next score MMA can
-      // start while the peer's partial is still on its way
-      const uint32_t reg = tR + 64 * (i % kRegions);
-      if (!warp_wait(c, kBarSFull + i % kRegions, (i / kRegions) & 1)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t own[32];
-      tmem_ld_32x32b_x32(reg + 32 * half, own);
-      tmem_wait_ld();
-      tc_fence_before();  // ordered before the row-max handshake that precedes P(i) stores
-      // the peer's partial for this warp's key columns (column half `half`)
-      if (!warp_wait_cluster(c, kBarRecvFull + half, i & 1)) { ok = false; break; }
-      // arm this half's next phase before the buffer is freed (the peer copies
-      // into it only after that), so each phase is armed exactly once
-      if (lane == 0 && q == 0 && i + 1 < p.n_tiles) mbar_arrive_expect_tx(c.bar(kBarRecvFull + half), kXchgBytes);
-      float s[32];
-      const uint32_t slot = c.sbase + kOffRecv;
-      uint32_t dep = 0;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float4 v = lds16f(slot + xchg_offset(h, k));
-        s[4 * k + 0] = __uint_as_float(own[4 * k + 0]) + v.x;
-        s[4 * k + 1] = __uint_as_float(own[4 * k + 1]) + v.y;
-        s[4 * k + 2] = __uint_as_float(own[4 * k + 2]) + v.z;
-        s[4 * k + 3] = __uint_as_float(own[4 * k + 3]) + v.w;
-        dep ^= __float_as_uint(v.x) ^ __float_as_uint(v.w);
-      }
-      // Free the slot for the peer.  The arrive's address depends on every
-      // loaded value (dep & dep_zero, a run-time 0), so it cannot issue
-      // before the loads have returned and needs no release fence.
-      mbar_arrive_remote_relaxed(mapa_shared(c.bar(kBarPeerFree + half), peer) + (dep & dep_zero));
-      // mask (waiting on the stage barrier acquires the gather's validity bits) and scale
-      if (!warp_wait(c, kBarFull + (i % kStages), (i / kStages) & 1)) { ok = false; break; }
-      const uint32_t vm = static_cast<uint32_t>(vmask[i % kStages] >> (32 * half));
-      if (!raw_max) {
-#pragma unroll
-        for (int k = 0; k < 32; ++k) s[k] *= scl;
-      }
-      float mx = -INFINITY;
-#pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        s[k] = ((vm >> k) & 1u) ? s[k] : -INFINITY;
-        mx = fmaxf(mx, s[k]);
-      }
-      // Row max across the two column halves of head h: post, wait until both
-      // posted, read.  Tile i uses slot i % 2, so a slot is rewritten only two
-      // tiles later, after the partner has passed the next handshake (and so
-      // has read it).
-      float* slot_p = pair + (i & 1) * 2 * kHeads;
-      slot_p[half * kHeads + h] = mx;
-      mbar_arrive(c.bar(kBarPairA + q));
-      if (!warp_wait(c, kBarPairA + q, i & 1)) { ok = false; break; }
-      mx = fmaxf(mx, slot_p[(half ^ 1) * kHeads + h]) * mul;  // log2-scaled row max of the tile
-      // Lazy rescale: m only moves when the tile max exceeds it by more than 8
-      // (log2 units), so P stays below 2^8 and O is rescaled rarely.
-      const bool grow = mx > m + 8.f;
-      const float f = grow ? fast_exp2(m - mx) : 1.f;  // m = -inf -> 0
-      if (grow) {
-        l *= f;
-        m = mx;
-      }
-      if (__any_sync(0xffffffffu, grow) && i > 0) {
-        // O may only be rescaled once P(i-1).V has been accumulated into it
-        if (!warp_wait(c, kBarPvDone + (i - 1) % kRegions, ((i - 1) / kRegions) & 1)) { ok = false; break; }
+  int pa = 0;  // uses of the row-max / row-sum pair barrier so far (its phase)
+  for (int mt = 0; mt < c.ntok; ++mt) {
+    const int64_t qrow = static_cast<int64_t>(token_of(p, c, mt)) * p.n_q + h;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int i = 0; i < p.n_tiles; ++i) {
+      const int j = mt * p.n_tiles + i;  // position in the cluster's tile stream
+      {
+        // own partial score tile i, read out at once so the next score MMA can
+        // start while the peer's partial is still on its way
+        const uint32_t reg = tR + 64 * (j % kRegions);
+        if (!warp_wait(c, kBarSFull + j % kRegions, (j / kRegions) & 1)) { ok = false; break; }
         tc_fence_after();
-#pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t o[32];
-          tmem_ld_32x32b_x32(tO + 32 * ch, o);
-          tmem_wait_ld();
+        uint32_t own[32];
+        tmem_ld_32x32b_x32(reg + 32 * half, own);
+        tmem_wait_ld();
+        tc_fence_before();  // ordered before the row-max handshake that precedes P(i) stores
+        // the peer's partial for this warp's key columns (column half `half`)
+        if (!warp_wait_cluster(c, kBarRecvFull + half, j & 1)) { ok = false; break; }
+        // arm this half's next phase before the buffer is freed (the peer copies
+        // into it only after that), so each phase is armed exactly once
+        if (lane == 0 && q == 0 && j + 1 < c.total) mbar_arrive_expect_tx(c.bar(kBarRecvFull + half), kXchgBytes);
+        float s[32];
+        const uint32_t slot = c.sbase + kOffRecv;
+        uint32_t dep = 0;
 #pragma unroll
-          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
-          tmem_st_32x32b_x32(tO + 32 * ch, o);
+        for (int k = 0; k < 8; ++k) {
+          const float4 v = lds16f(slot + xchg_offset(h, k));
+          s[4 * k + 0] = __uint_as_float(own[4 * k + 0]) + v.x;
+          s[4 * k + 1] = __uint_as_float(own[4 * k + 1]) + v.y;
+          s[4 * k + 2] = __uint_as_float(own[4 * k + 2]) + v.z;
+          s[4 * k + 3] = __uint_as_float(own[4 * k + 3]) + v.w;
+          dep ^= __float_as_uint(v.x) ^ __float_as_uint(v.w);
         }
-        tmem_wait_st();
-      }
-      const float mm = (m == -INFINITY) ? 0.f : m;
-      uint32_t phi[16], plo[16];
-      float lsum = 0.f;
+        // Free the slot for the peer.  The arrive's address depends on every
+        // loaded value (dep & dep_zero, a run-time 0), so it cannot issue
+        // before the loads have returned and needs no release fence.
+        mbar_arrive_remote_relaxed(mapa_shared(c.bar(kBarPeerFree + half), peer) + (dep & dep_zero));
+        // mask (waiting on the stage barrier acquires the gather's validity bits) and scale
+        if (!warp_wait(c, kBarFull + (j % kStages), (j / kStages) & 1)) { ok = false; break; }
+        const uint32_t vm = static_cast<uint32_t>(vmask[j % kStages] >> (32 * half));
+        if (!raw_max) {
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const float p0 = fast_exp2(fmaf(s[2 * k], mul, -mm));
-        const float p1 = fast_exp2(fmaf(s[2 * k + 1], mul, -mm));
-        lsum += p0 + p1;
-        const uint32_t hw = pack_bf16x2(p0, p1);
-        phi[k] = hw;
-        // p - bf16(p) is exact in fp32; its bf16 rounding leaves an error <= 2^-18 p
-        plo[k] = pack_bf16x2(p0 - __uint_as_float(hw << 16), p1 - __uint_as_float(hw & 0xFFFF0000u));
-      }
-      l += lsum;
-      // P(i) overwrites S(i) in its region: the senders must have read it out
-      // (this warp and its pair partner read their own columns before the
-      // row-max handshake above)
-      if (!warp_wait(c, kBarSFree + i % kRegions, (i / kRegions) & 1)) { ok = false; break; }
-      tc_fence_after();
-      tmem_st_32x32b_x16(reg + 16 * half, phi);
-      tmem_st_32x32b_x16(reg + 32 + 16 * half, plo);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(c.bar(kBarPFull + i % kRegions));
-    }
-  }
-  if (!ok) return;
-  // l over the whole row: add the partner's column half (same order in both threads)
-  float* slot_l = pair + (p.n_tiles & 1) * 2 * kHeads;
-  slot_l[half * kHeads + h] = l;
-  mbar_arrive(c.bar(kBarPairA + q));
-  if (!warp_wait(c, kBarPairA + q, p.n_tiles & 1)) return;
-  const float l_tot = half == 0 ? l + slot_l[kHeads + h] : slot_l[h] + l;
-  if (!warp_wait(c, kBarPvDone + (p.n_tiles - 1) % kRegions, ((p.n_tiles - 1) / kRegions) & 1)) return;
-  tc_fence_after();
-  const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
-  uint4* op = reinterpret_cast<uint4*>(p.out + qrow * 512 + c.crank * 256 + half * 128);
+          for (int k = 0; k < 32; ++k) s[k] *= scl;
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          s[k] = ((vm >> k) & 1u) ? s[k] : -INFINITY;
+          mx = fmaxf(mx, s[k]);
+        }
+        // Row max across the two column halves of head h: post, wait until both
+        // posted, read.  Use pa of the pair barrier (one per tile, one per
+        // token's row sum) takes slot pa % 2, so a slot is rewritten only two
+        // uses later, after the partner has passed the next handshake (and so
+        // has read it).
+        float* slot_p = pair + (pa & 1) * 2 * kHeads;
+        slot_p[half * kHeads + h] = mx;
+        mbar_arrive(c.bar(kBarPairA + q));
+        if (!warp_wait(c, kBarPairA + q, pa & 1)) { ok = false; break; }
+        ++pa;
+        mx = fmaxf(mx, slot_p[(half ^ 1) * kHeads + h]) * mul;  // log2-scaled row max of the tile
+        // Lazy rescale: m only moves when the tile max exceeds it by more than 8
+        // (log2 units), so P stays below 2^8 and O is rescaled rarely.
+        const bool grow = mx > m + 8.f;
+        const float f = grow ? fast_exp2(m - mx) : 1.f;  // m = -inf -> 0
+        if (grow) {
+          l *= f;
+          m = mx;
+        }
+        if (__any_sync(0xffffffffu, grow) && i > 0) {
+          // O may only be rescaled once P(j-1).V has been accumulated into it
+          if (!warp_wait(c, kBarPvDone + (j - 1) % kRegions, ((j - 1) / kRegions) & 1)) { ok = false; break; }
+          tc_fence_after();
 #pragma unroll 1
-  for (int ch = 0; ch < 4; ++ch) {
-    uint32_t o[32];
-    tmem_ld_32x32b_x32(tO + 32 * ch, o);
-    tmem_wait_ld();
-    if (live) {
+          for (int ch = 0; ch < 4; ++ch) {
+            uint32_t o[32];
+            tmem_ld_32x32b_x32(tO + 32 * ch, o);
+            tmem_wait_ld();
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        uint4 w;
-        w.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l);
-        w.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l);
-        w.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l);
-        w.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l);
-        op[ch * 4 + k] = w;
+            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
+            tmem_st_32x32b_x32(tO + 32 * ch, o);
+          }
+          tmem_wait_st();
+        }
+        const float mm = (m == -INFINITY) ? 0.f : m;
+        uint32_t phi[16], plo[16];
+        float lsum = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float p0 = fast_exp2(fmaf(s[2 * k], mul, -mm));
+          const float p1 = fast_exp2(fmaf(s[2 * k + 1], mul, -mm));
+          lsum += p0 + p1;
+          const uint32_t hw = pack_bf16x2(p0, p1);
+          phi[k] = hw;
+          // p - bf16(p) is exact in fp32; its bf16 rounding leaves an error <= 2^-18 p
+          plo[k] = pack_bf16x2(p0 - __uint_as_float(hw << 16), p1 - __uint_as_float(hw & 0xFFFF0000u));
+        }
+        l += lsum;
+        // P(i) overwrites S(i) in its region: the senders must have read it out
+        // (this warp and its pair partner read their own columns before the
+        // row-max handshake above)
+        if (!warp_wait(c, kBarSFree + j % kRegions, (j / kRegions) & 1)) { ok = false; break; }
+        tc_fence_after();
+        tmem_st_32x32b_x16(reg + 16 * half, phi);
+        tmem_st_32x32b_x16(reg + 32 + 16 * half, plo);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(c.bar(kBarPFull + j % kRegions));
+      }
+
+    }
+    if (!ok) return;
+    if (mt + 1 < c.ntok) {
+      // the next token's Q replaces this one's once its score MMAs are complete
+      if (!warp_wait(c, kBarQFree, mt & 1)) return;
+      tc_fence_after();
+      load_q(p, c, h, half, live, static_cast<int64_t>(token_of(p, c, mt + 1)) * p.n_q + h, tQ);
+    }
+    // l over the whole row: add the partner's column half (same order in both threads)
+    float* slot_l = pair + (pa & 1) * 2 * kHeads;
+    slot_l[half * kHeads + h] = l;
+    mbar_arrive(c.bar(kBarPairA + q));
+    if (!warp_wait(c, kBarPairA + q, pa & 1)) return;
+    ++pa;
+    const float l_tot = half == 0 ? l + slot_l[kHeads + h] : slot_l[h] + l;
+    const int jl = (mt + 1) * p.n_tiles - 1;  // the token's last tile
+    if (!warp_wait(c, kBarPvDone + jl % kRegions, (jl / kRegions) & 1)) return;
+    tc_fence_after();
+    const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
+    uint4* op = reinterpret_cast<uint4*>(p.out + qrow * 512 + c.crank * 256 + half * 128);
+#pragma unroll 1
+    for (int ch = 0; ch < 4; ++ch) {
+      uint32_t o[32];
+      tmem_ld_32x32b_x32(tO + 32 * ch, o);
+      tmem_wait_ld();
+      if (live) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l);
+          w.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l);
+          w.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l);
+          w.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l);
+          op[ch * 4 + k] = w;
+        }
       }
     }
+    // O is in registers: the next token's first P.V may overwrite it
+    tc_fence_before();
+    mbar_arrive(c.bar(kBarOFree));
+    if (live && c.crank == 0 && half == 0 && p.lse != nullptr)
+      p.lse[qrow] = l_tot > 0.f ? (m + log2f(l_tot)) * 0.69314718055994530942f : -INFINITY;
   }
-  if (live && c.crank == 0 && half == 0 && p.lse != nullptr)
-    p.lse[qrow] = l_tot > 0.f ? (m + log2f(l_tot)) * 0.69314718055994530942f : -INFINITY;
 }
 
 // ------------------------------------------------------------------ kernel
@@ -703,7 +791,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_spa
   c.smem = smem;
   c.sbase = smem_u32(smem);
   c.crank = cluster_ctarank();
-  c.t = blockIdx.x >> 1;
+  c.cid = blockIdx.x >> 1;
+  c.ntok = (p.T - c.cid + p.n_clusters - 1) / p.n_clusters;
+  c.total = c.ntok * p.n_tiles;
   c.abort = reinterpret_cast<volatile uint32_t*>(smem + kOffAbort);
   if (tid == 0) {
     // the swizzled operand layouts need a 1024-byte aligned base
@@ -730,17 +820,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_spa
     }
     for (int q = 0; q < 4; ++q) mbar_init(c.bar(kBarPairA + q), 64);
     mbar_init(c.bar(kBarQReady), kSoftmaxThreads);
+    mbar_init(c.bar(kBarQFree), 1);
+    mbar_init(c.bar(kBarOFree), kSoftmaxThreads);
     mbar_init(c.bar(kBarFinal), 1);
     fence_mbarrier_init_cluster();
     for (int h2 = 0; h2 < 2; ++h2) mbar_arrive_expect_tx(c.bar(kBarRecvFull + h2), kXchgBytes);
     *reinterpret_cast<volatile uint32_t*>(smem + kOffZero) = 0u;
+    *reinterpret_cast<volatile int*>(smem + kOffTotal) = c.total;
   }
   // the index warps issue their first top-k loads before the set-up barrier
-  int idx0[8], act0 = 0;
-  if (warp >= kIndexWarp && warp < kIndexWarp + kIndexWarps) {
-    act0 = __ldg(p.act_seqs + c.t / p.S1);
-    index_load(p, p.topk_idx + static_cast<int64_t>(c.t) * p.topk, (warp - kIndexWarp) * kIdxBatch, lane, idx0);
-  }
+  int idx0[8];
+  if (warp >= kIndexWarp && warp < kIndexWarp + kIndexWarps)
+    index_load(p, c, (warp - kIndexWarp) * kIdxBatch, lane, idx0);
   if (warp == kMmaWarp) {
     tmem_alloc(c.sbase + kOffTmemSlot, kTmemCols);
     tmem_relinquish();
@@ -766,7 +857,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_spa
         if (lane == 0) mma_role(p, c);
         __syncwarp();
       } else if (warp < kIndexWarp + kIndexWarps) {
-        index_role(p, c, warp - kIndexWarp, lane, idx0, act0);
+        index_role(p, c, warp - kIndexWarp, lane, idx0);
       }
     }
   }
@@ -803,6 +894,9 @@ constexpr int kMaxDevices = 64;
 std::once_flag g_attr_once[kMaxDevices][2];
 cudaError_t g_attr_err[kMaxDevices][2];
 
+int g_max_clusters[kMaxDevices][2];
+
+// Also records how many two-CTA clusters of the kernel the device runs at once.
 template <bool kInt8>
 cudaError_t prepare_kernel(int dev) {
   std::call_once(g_attr_once[dev][kInt8 ? 1 : 0], [dev] {
@@ -817,6 +911,23 @@ cudaError_t prepare_kernel(int dev) {
       const long need = 256L * R::kSoftmax + 128L * 80 + 256L * R::kGather + 128L * R::kControl;
       if (e == cudaSuccess && (fa.numRegs < 80 || static_cast<long>(fa.numRegs) * mlasp::kThreads < need))
         e = cudaErrorInvalidConfiguration;
+    }
+    if (e == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(2, 1, 1);
+      cfg.blockDim = dim3(mlasp::kThreads, 1, 1);
+      cfg.dynamicSmemBytes = mlasp::kSmemBytes;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, mlasp::mla_sparse_fwd_kernel<kInt8>, &cfg);
+      g_max_clusters[dev][kInt8 ? 1 : 0] = n;
+      if (e == cudaSuccess && n < 1) e = cudaErrorInvalidConfiguration;
     }
     g_attr_err[dev][kInt8 ? 1 : 0] = e;
   });
@@ -888,7 +999,12 @@ mla_status mla_sparse_attn_fwd(const mla_dims* dims, const void* q_nope, const v
   p.mbps = d.max_blocks_per_seq;
   p.n_tiles = (d.topk + mlasp::kTileKeys - 1) / mlasp::kTileKeys;
   p.scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634);
-  const dim3 grid(static_cast<unsigned>(2 * T));
+  // persistent clusters: as many as run at once (never more than tokens); cluster
+  // c takes tokens c, c + n_clusters, ... as one stream of key tiles
+  const int max_clusters = g_max_clusters[dev][int8 ? 1 : 0];
+  p.T = static_cast<int>(T);
+  p.n_clusters = static_cast<int>(T < max_clusters ? T : max_clusters);
+  const dim3 grid(static_cast<unsigned>(2 * p.n_clusters));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (int8)
     mlasp::mla_sparse_fwd_kernel<true><<<grid, mlasp::kThreads, mlasp::kSmemBytes, s>>>(p);

@@ -187,3 +187,38 @@ def test_deterministic_and_permutation_stable():
 def test_full_size_workload_sampled(name):
     inp = workloads.NAMED[name]()
     check_sampled(inp, name, n_sample=6)
+
+
+# ------------------------------------------------------------ persistent clusters: token streams
+# The kernel runs at most as many two-CTA clusters as the GPU holds at once
+# (76 on GB300); cluster c takes tokens c, c + G, ... as one stream of key
+# tiles.  These cases move the token boundaries through the stream.
+@pytest.mark.parametrize("kv_int8", [False, True])
+def test_one_tile_per_token_long_streams(kv_int8):
+    """topk = 64: every tile is a token boundary (Q reload, O hand-off and the
+    row-sum handshake on every tile); 1200 tokens, ~16 per cluster."""
+    B, S1 = 600, 2
+    act = np.random.default_rng(40).integers(1, 400, size=B)
+    inp = workloads.make_inputs(B=B, S1=S1, n_q=128, act_seqs=act, topk=64, seed=40, kv_int8=kv_int8)
+    check_full(inp, f"one tile per token int8={kv_int8}")
+
+
+@pytest.mark.parametrize("B", [38, 39, 77])
+def test_token_counts_around_the_cluster_count(B):
+    """T = 76, 78 and 154 tokens: one token per cluster, two clusters with a
+    second token, and every cluster with two or three; topk 100 leaves a
+    partial last tile in every token."""
+    inp = workloads.make_inputs(B=B, S1=2, n_q=128, act_seqs=[700] * B, topk=100, seed=41 + B)
+    check_full(inp, f"T={2 * B}")
+
+
+def test_rescale_inside_a_later_token_of_the_stream():
+    """Large logits in tokens that are a cluster's second or third: the O
+    rescale must act on the accumulator of the current token only."""
+    B = 100
+    inp = workloads.make_inputs(B=B, S1=2, n_q=64, act_seqs=[600] * B, topk=192, seed=45)
+    q = inp["q_nope"].astype(np.int32)
+    nz = (q & 0x7FFF) != 0
+    scaled = np.where(nz, q + (4 << 7), q).astype(np.uint16)  # x16, exact in bf16
+    inp["q_nope"][160:] = scaled[160:]
+    check_full(inp, "rescale in later tokens")

@@ -66,7 +66,9 @@ size_t mla_indexer_workspace_bytes(const mla_indexer_dims* dims);
  *             candidate positions j, -inf for positions below act_seqs[b] that
  *             are not candidates, unspecified at and beyond act_seqs[b].
  * Two launches on `stream` (mla_indexer_scores into the workspace, then
- * mla_indexer_select).  MLA_ERR_SHAPE when the workspace is too small.
+ * mla_indexer_select as a programmatic dependent launch, so its launch
+ * overlaps the score grid's tail).  MLA_ERR_SHAPE when the workspace is too
+ * small.
  */
 mla_status mla_indexer_topk(const mla_indexer_dims* dims, const void* q, const float* w, const void* k_cache,
                             const int32_t* block_table, const int32_t* act_seqs, int32_t* topk_idx,

@@ -188,6 +188,9 @@ idx_scores_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmemSlot);
+  // a selection grid launched behind this one may be scheduled now; it waits
+  // for this grid's completion before it reads any score
+  if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t qrow0 = static_cast<int64_t>(b) * p.N;  // the sequence's (token, head) rows are contiguous
 
   if (!*c.abort) {
@@ -374,6 +377,9 @@ __global__ void __launch_bounds__(kSelThreads) idx_topk_kernel(const SelectParam
   int32_t* out = p.topk_idx + static_cast<int64_t>(t) * p.topk;
   const uint32_t topk = static_cast<uint32_t>(p.topk);
 
+  // When launched behind the score grid (programmatic dependent launch), wait
+  // for it to complete and its scores to be visible; otherwise a no-op.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   float vreg[kRegChunks];
 #pragma unroll
   for (int c = 0; c < kRegChunks; ++c) {
@@ -821,9 +827,11 @@ mla_status launch_scores(const mla_indexer_dims& d, int dev, const void* q, cons
   return MLA_OK;
 }
 
-// Launches the selection kernel (arguments already checked).
+// Launches the selection kernel (arguments already checked).  `behind_scores`:
+// it directly follows the score kernel on `s`, so it may be launched as a
+// programmatic dependent (its launch overlaps the score grid's tail).
 mla_status launch_select(const mla_indexer_dims& d, const float* scores, const int32_t* act_seqs, int32_t* topk_idx,
-                         cudaStream_t s) {
+                         cudaStream_t s, bool behind_scores) {
   mlaidx::SelectParams sel;
   sel.scores = scores;
   sel.ld = static_cast<int64_t>(d.max_blocks_per_seq) * 128;
@@ -831,8 +839,18 @@ mla_status launch_select(const mla_indexer_dims& d, const float* scores, const i
   sel.act_seqs = act_seqs;
   sel.topk_idx = topk_idx;
   sel.topk = d.topk;
-  mlaidx::idx_topk_kernel<<<static_cast<unsigned>(d.B * d.S1), mlaidx::kSelThreads, 0, s>>>(sel);
-  const cudaError_t e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(d.B * d.S1), 1, 1);
+  cfg.blockDim = dim3(mlaidx::kSelThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = behind_scores ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, mlaidx::idx_topk_kernel, sel);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return idx_fail(MLA_ERR_CUDA, "selection kernel launch: %s", cudaGetErrorString(e));
   return MLA_OK;
 }
@@ -861,7 +879,7 @@ mla_status mla_indexer_select(const mla_indexer_dims* dims, const float* scores,
   g_idx_error[0] = '\0';
   const mla_status st = check_select_args(dims, scores, act_seqs, topk_idx);
   if (st != MLA_OK) return st;
-  return launch_select(*dims, scores, act_seqs, topk_idx, static_cast<cudaStream_t>(stream));
+  return launch_select(*dims, scores, act_seqs, topk_idx, static_cast<cudaStream_t>(stream), false);
 }
 
 mla_status mla_indexer_topk(const mla_indexer_dims* dims, const void* q, const float* w, const void* k_cache,
@@ -876,7 +894,7 @@ mla_status mla_indexer_topk(const mla_indexer_dims* dims, const void* q, const f
   float* scores = static_cast<float*>(workspace);
   st = launch_scores(*dims, dev, q, w, k_cache, block_table, act_seqs, scores, s);
   if (st != MLA_OK) return st;
-  return launch_select(*dims, scores, act_seqs, topk_idx, s);
+  return launch_select(*dims, scores, act_seqs, topk_idx, s, true);
 }
 
 // For callers that cannot allocate device memory at call time, e.g. a host
@@ -919,7 +937,7 @@ mla_status mla_indexer_topk_noalloc(const mla_indexer_dims* dims, const void* q,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   st = launch_scores(*dims, dev2, q, w, k_cache, block_table, act_seqs, scratch, s);
   if (st != MLA_OK) return st;
-  return launch_select(*dims, scratch, act_seqs, topk_idx, s);
+  return launch_select(*dims, scratch, act_seqs, topk_idx, s, true);
 }
 
 mla_status mla_indexer_device_status(void* stream, uint32_t* flags, int32_t clear) {

@@ -4,8 +4,8 @@ the Lightning Indexer's top-k selection and for the paged cache writer.
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
 leg may import this package.  The CUDA product path never imports it and the
 two share no code.  The arithmetic lives in ``mla_oracle.c``,
-``indexer_oracle.c`` and ``cache_oracle.c`` (see their headers for the passages
-they follow); this
+``indexer_oracle.c``, ``cache_oracle.c`` and ``swa_oracle.c`` (see their
+headers for the passages they follow); this
 module only compiles them and marshals numpy arrays through ctypes.
 """
 from __future__ import annotations
@@ -18,7 +18,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRCS = [os.path.join(_HERE, "mla_oracle.c"), os.path.join(_HERE, "indexer_oracle.c"),
-         os.path.join(_HERE, "cache_oracle.c")]
+         os.path.join(_HERE, "cache_oracle.c"), os.path.join(_HERE, "swa_oracle.c")]
 _LIB_PATH = os.path.join(_HERE, "libmla_oracle.so")
 _lib = None
 
@@ -52,6 +52,8 @@ def _load():
         lib.idx_oracle_select.restype = I
         lib.cache_oracle_write.argtypes = [I, I, ctypes.c_int64, P, P, P, P, P, P, ctypes.POINTER(ctypes.c_int64)]
         lib.cache_oracle_write.restype = I
+        lib.swa_oracle_window_lists.argtypes = [I, I, P, I, P]
+        lib.swa_oracle_window_lists.restype = I
         _lib = lib
     return _lib
 
@@ -178,3 +180,23 @@ def cache_write(k_nope, k_rope, cache_index, kv_nope, kv_rope, kv_scales=None, i
     if rc != 0:
         raise ValueError(f"cache_oracle_write rejected the arguments ({rc})")
     return kn, kr, ks, int(bad.value)
+
+
+def swa_window_lists(act_seqs, S1: int, window: int):
+    """Each token's window positions (B*S1, window) int32, -1 where negative."""
+    lib = _load()
+    act = np.ascontiguousarray(act_seqs, dtype=np.int32)
+    B = int(act.shape[0])
+    lists = np.empty((B * S1, window), dtype=np.int32)
+    if lib.swa_oracle_window_lists(B, S1, _ptr(act), int(window), _ptr(lists)) != 0:
+        raise ValueError("swa_oracle_window_lists rejected the arguments")
+    return lists
+
+
+def swa_forward(inp: dict, window: int, tokens=None, threads: int = 0):
+    """Sliding-window attention: the window lists, then the attention
+    definition over them (``forward`` with top-k = the window)."""
+    d = dict(inp["dims"])
+    d["topk"] = int(window)
+    lists = swa_window_lists(inp["act_seqs"], d["S1"], window)
+    return forward(dict(inp, dims=d, topk_idx=lists), tokens=tokens, threads=threads)

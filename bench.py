@@ -67,6 +67,17 @@ def row_bytes(inp):
     return (512 + 4 * 4 + 128) if inp["dims"]["kv_int8"] else (1024 + 128)
 
 
+def window_positions(inp):
+    """For the sliding-window workload: each token's window positions (the
+    same rule as the window entry point), used only to count bytes and flops."""
+    d = inp["dims"]
+    W = inp["window"]
+    act = np.repeat(inp["act_seqs"].astype(np.int64), d["S1"])
+    p = act - d["S1"] + np.tile(np.arange(d["S1"]), d["B"])
+    lists = p[:, None] - W + 1 + np.arange(W)[None, :]
+    return np.where(lists >= 0, lists, -1)
+
+
 def valid_mask(inp):
     d = inp["dims"]
     act = np.repeat(inp["act_seqs"], d["S1"])[:, None]
@@ -75,7 +86,10 @@ def valid_mask(inp):
 
 
 def algorithmic_counts(inp):
-    """Method's own work: SURVEY-style counts from the actual inputs."""
+    """Method's own work: counts from the actual inputs."""
+    if "window" in inp:
+        inp = dict(inp, topk_idx=window_positions(inp).astype(np.int32),
+                   dims=dict(inp["dims"], topk=int(inp["window"])))
     d = inp["dims"]
     T, H = d["B"] * d["S1"], d["n_q"]
     vm = valid_mask(inp)
@@ -127,7 +141,7 @@ def ncu_traffic(workload, kernel=KERNEL_NAME, source=KERNEL_SOURCE):
     return float(mt.group(1))
 
 
-SEEDS = {"tiny_decode": 0, "mtp_decode": 1, "int8_decode": 2, "varlen_decode": 3, "prefill": 4,
+SEEDS = {"tiny_decode": 0, "mtp_decode": 1, "int8_decode": 2, "varlen_decode": 3, "prefill": 4, "swa_decode": 10,
          "indexer_decode": 5, "indexer_tiny": 6, "indexer_varlen": 7, "cache_write_decode": 8,
          "cache_write_prefill": 9}
 
@@ -149,10 +163,18 @@ def reduce_max_over_ranks(values, device):
     return [float(v) for v in t.cpu()]
 
 
-def run_config(workload, d, world):
+SWA_METRIC = "sliding-window MLA attn µs/call, % HBM roofline (B64 S1=2, window 128)"
+
+
+def metric_of(inp):
+    return SWA_METRIC if "window" in inp else METRIC
+
+
+def run_config(workload, d, world, window=None):
     """The ``config`` object of the JSON line (the same for both arms)."""
-    return {
-        "workload": f"{workload}: B={d['B']} S1={d['S1']} N_Q={d['n_q']} topk={d['topk']} "
+    sel = f"window={window} (sliding)" if window else f"topk={d['topk']}"
+    cfg = {
+        "workload": f"{workload}: B={d['B']} S1={d['S1']} N_Q={d['n_q']} {sel} "
                     f"{'int8' if d['kv_int8'] else 'bf16'} paged cache ({d['num_blocks']} blocks of 128)",
         "B": d["B"], "S1": d["S1"], "n_q": d["n_q"], "topk": d["topk"],
         "kv_dtype": "int8" if d["kv_int8"] else "bf16",
@@ -160,6 +182,10 @@ def run_config(workload, d, world):
         "launch": "a bounded GPU spin precedes each timed call, so its events time the device, not the host launch",
         "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
     }
+    if window:
+        cfg["window"] = window
+        del cfg["topk"]
+    return cfg
 
 
 # ------------------------------------------------------------------ timing helpers
@@ -241,6 +267,15 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ CPU oracle sample
+def oracle_call(inp, tokens=None):
+    """The oracle for this workload: the sliding-window oracle when it has a
+    window, the sparse-attention oracle otherwise."""
+    import oracle
+    if "window" in inp:
+        return oracle.swa_forward(inp, inp["window"], tokens=tokens)
+    return oracle.forward(inp, tokens=tokens)
+
+
 def time_oracle(inp, target_s: float):
     """Time the oracle, as it stands, on a bounded token sample; returns
     (us per full call, cores, sample description)."""
@@ -251,19 +286,19 @@ def time_oracle(inp, target_s: float):
     # one token per thread: the time of one parallel wave
     wave = min(T, cores)
     t0 = time.perf_counter()
-    oracle.forward(inp, tokens=list(range(wave)))
+    oracle_call(inp, tokens=list(range(wave)))
     t_wave = max(time.perf_counter() - t0, 1e-6)
     full_est = t_wave * math.ceil(T / wave)
     if full_est <= target_s:
         reps = max(1, int(round(target_s / full_est)))
         t0 = time.perf_counter()
         for _ in range(reps):
-            oracle.forward(inp)
+            oracle_call(inp)
         dt = time.perf_counter() - t0
         return dt / reps * 1e6, cores, f"all {T} tokens, {reps} oracle calls ({dt:.2f} s)"
     n = int(min(T, max(wave, round(target_s / t_wave) * wave)))
     t0 = time.perf_counter()
-    oracle.forward(inp, tokens=list(range(n)))
+    oracle_call(inp, tokens=list(range(n)))
     dt = time.perf_counter() - t0
     return dt / n * T * 1e6, cores, f"first {n} of {T} tokens in one oracle call ({dt:.2f} s), scaled to all {T} tokens"
 
@@ -306,10 +341,17 @@ def main():
     stream = torch.cuda.current_stream()
     mode = inp.get("mode", "decode")
 
+    window = inp.get("window")
+
     def launch():
-        mla.mla_sparse_attn_fwd(dev["q_nope"], dev["q_rope"], dev["kv_nope"], dev["kv_rope"], dev["kv_scales"],
-                                dev["topk_idx"], dev["block_table"], dev["act_seqs"], dev["out"], dev["lse"],
-                                softmax_scale=inp["softmax_scale"], mode=mode, dims=dims, stream=stream)
+        if window:
+            mla.mla_swa_fwd(dev["q_nope"], dev["q_rope"], dev["kv_nope"], dev["kv_rope"], dev["kv_scales"],
+                            dev["block_table"], dev["act_seqs"], dev["out"], dev["lse"], window=window,
+                            softmax_scale=inp["softmax_scale"], mode=mode, dims=dims, stream=stream)
+        else:
+            mla.mla_sparse_attn_fwd(dev["q_nope"], dev["q_rope"], dev["kv_nope"], dev["kv_rope"], dev["kv_scales"],
+                                    dev["topk_idx"], dev["block_table"], dev["act_seqs"], dev["out"], dev["lse"],
+                                    softmax_scale=inp["softmax_scale"], mode=mode, dims=dims, stream=stream)
 
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
     for i in range(max(3, args.warmup)):
@@ -378,7 +420,7 @@ def main():
         traffic = ncu_traffic(args.workload)
         d = inp["dims"]
         line = {
-            "metric": METRIC,
+            "metric": metric_of(inp),
             "value": round(us, 3),
             "unit": UNIT,
             "n_gpus": world,
@@ -390,7 +432,7 @@ def main():
             "vs_baseline": None,
             "dtype": "bf16",
             "data": "synthetic",
-            "config": run_config(args.workload, d, world),
+            "config": run_config(args.workload, d, world, inp.get("window")),
             "gathered_kv_tbps": round(counts["gathered_bytes"] * world / (us * 1e-6) / 1e12, 4),
             "tflops": round(tflops * world, 2),
             "roofline_us": round(roofline_us, 3),
@@ -859,20 +901,20 @@ def run_reference(args, world, rank):
     cores = oracle.max_threads()
     toks_per_step = max(1, cores)
     if args.warmup > 0:
-        oracle.forward(inp, tokens=[0])
+        oracle_call(inp, tokens=[0])
     per_call = []
     for i in range(args.steps):
         toks = [(i * toks_per_step + k) % T for k in range(toks_per_step)]
         t0 = time.perf_counter()
-        oracle.forward(inp, tokens=toks)
+        oracle_call(inp, tokens=toks)
         per_call.append((time.perf_counter() - t0) / len(toks) * T * 1e6)
     us = float(np.mean(per_call))
     sample = f"{toks_per_step} of {T} tokens per step, scaled to all {T} tokens"
     line = {
-        "metric": METRIC, "value": round(us, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": metric_of(inp), "value": round(us, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(us / 1000.0, 3), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-        "config": run_config(args.workload, d, world),
+        "config": run_config(args.workload, d, world, inp.get("window")),
         "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }

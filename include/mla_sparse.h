@@ -121,6 +121,22 @@ mla_status mla_sparse_attn_fwd(const mla_dims* dims, const void* q_nope, const v
                                const int32_t* act_seqs, void* out, float* lse, float softmax_scale,
                                int32_t mode, void* stream);
 
+/*
+ * mla_swa_fwd -- sliding-window attention over the same paged cache ("NPU
+ * DeepSeek-V4 PyPTO fused-operator optimization", section SWA: attention over
+ * the original KV with a sliding-window mask, for prefill and MTP).  The S1
+ * query tokens of sequence b are its newest S1 positions: token (b, s) sits at
+ * p = act_seqs[b] - S1 + s and attends to the positions [p - window + 1, p]
+ * that are >= 0.  The pages give no window size: `window` (>= 1) is the
+ * caller's.  Arguments as mla_sparse_attn_fwd without topk_idx; dims->topk is
+ * ignored.  Same kernel, with each token's position list built on the device
+ * instead of read.
+ */
+mla_status mla_swa_fwd(const mla_dims* dims, const void* q_nope, const void* q_rope, const void* kv_nope,
+                       const void* kv_rope, const float* kv_scales, const int32_t* block_table,
+                       const int32_t* act_seqs, int32_t window, void* out, float* lse, float softmax_scale,
+                       int32_t mode, void* stream);
+
 /* Description of the last error on this thread ("" after a success). */
 const char* mla_sparse_last_error(void);
 

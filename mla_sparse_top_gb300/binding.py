@@ -24,7 +24,7 @@ MLA_KV_INT8 = 1
 MLA_DEVICE_BAD_BLOCK = 0x1
 MLA_DEVICE_TIMEOUT = 0x2
 
-EXPORTED_SYMBOLS = ("mla_sparse_attn_fwd", "mla_sparse_last_error", "mla_sparse_device_status",
+EXPORTED_SYMBOLS = ("mla_sparse_attn_fwd", "mla_swa_fwd", "mla_sparse_last_error", "mla_sparse_device_status",
                     "mla_sparse_abi_version", "mla_indexer_workspace_bytes", "mla_indexer_topk",
                     "mla_indexer_scores", "mla_indexer_select", "mla_indexer_device_status",
                     "mla_indexer_last_error", "mla_indexer_topk_noalloc", "mla_cache_write",
@@ -62,6 +62,9 @@ def load_library(path: str = LIB_PATH):
     vp = ctypes.c_void_p
     lib.mla_sparse_attn_fwd.argtypes = [ctypes.POINTER(MlaDims)] + [vp] * 10 + [ctypes.c_float, ctypes.c_int32, vp]
     lib.mla_sparse_attn_fwd.restype = ctypes.c_int
+    lib.mla_swa_fwd.argtypes = [ctypes.POINTER(MlaDims)] + [vp] * 7 + [ctypes.c_int32, vp, vp, ctypes.c_float,
+                                                                        ctypes.c_int32, vp]
+    lib.mla_swa_fwd.restype = ctypes.c_int
     lib.mla_sparse_last_error.argtypes = []
     lib.mla_sparse_last_error.restype = ctypes.c_char_p
     lib.mla_sparse_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int32]
@@ -146,6 +149,32 @@ def mla_sparse_attn_fwd(q_nope, q_rope, kv_nope, kv_rope, kv_scales, topk_idx, b
                                  _ptr(kv_scales if kv_int8 else None), _ptr(topk_idx), _ptr(block_table),
                                  _ptr(act_seqs), _ptr(out), _ptr(lse), ctypes.c_float(softmax_scale),
                                  ctypes.c_int32(int(mode)), _stream_handle(stream))
+    _check(st)
+    return out, lse
+
+
+def mla_swa_fwd(q_nope, q_rope, kv_nope, kv_rope, kv_scales, block_table, act_seqs, out, lse=None, *,
+                window: int, softmax_scale=None, mode: int | str = MLA_MODE_DECODE, S1: int = 1, stream=None,
+                dims: MlaDims | None = None):
+    """Enqueue one call of the C entry point with the same name: sliding-window
+    attention, token (b, s) at position act_seqs[b] - S1 + s attending to the
+    `window` positions ending at its own.  Tensors as mla_sparse_attn_fwd
+    without topk_idx."""
+    lib = load_library()
+    kv_int8 = kv_nope.dtype == torch.int8
+    if dims is None:
+        T, n_q, d_nope = q_nope.shape
+        dims = MlaDims(B=T // S1, S1=S1, n_q=n_q, n_kv=1, d_nope=d_nope, d_rope=64, block_size=128,
+                       num_blocks=kv_nope.shape[0] // 128, max_blocks_per_seq=block_table.shape[1], topk=window,
+                       kv_dtype=MLA_KV_INT8 if kv_int8 else MLA_KV_BF16)
+    if isinstance(mode, str):
+        mode = {"decode": MLA_MODE_DECODE, "prefill": MLA_MODE_PREFILL}[mode]
+    if softmax_scale is None:
+        softmax_scale = (dims.d_nope + dims.d_rope) ** -0.5
+    st = lib.mla_swa_fwd(ctypes.byref(dims), _ptr(q_nope), _ptr(q_rope), _ptr(kv_nope), _ptr(kv_rope),
+                         _ptr(kv_scales if kv_int8 else None), _ptr(block_table), _ptr(act_seqs),
+                         ctypes.c_int32(int(window)), _ptr(out), _ptr(lse), ctypes.c_float(softmax_scale),
+                         ctypes.c_int32(int(mode)), _stream_handle(stream))
     _check(st)
     return out, lse
 

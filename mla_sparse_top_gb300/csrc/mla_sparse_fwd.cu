@@ -163,6 +163,7 @@ struct Params {
   int S1, n_q, topk, num_blocks, mbps, n_tiles;
   int T;           // query tokens B * S1
   int n_clusters;  // clusters in the grid; cluster c takes tokens c, c + n_clusters, ...
+  int window;      // > 0: sliding window of this many positions instead of top-k lists (topk = window)
   float scale_log2;
 };
 
@@ -230,18 +231,33 @@ __device__ __forceinline__ int seq_of_tile(const Params& p, const Ctx& c, int jj
   return token_of(p, c, jj / p.n_tiles) / p.S1;
 }
 
-// top-k entries of the pass starting at stream tile j0 (-1 beyond the stream
-// or the list)
+// Entries (logical positions) of the pass starting at stream tile j0, -1
+// beyond the stream or the list: the token's top-k list, or with a sliding
+// window the positions p - window + 1 + e of the token at position
+// p = act_seqs[b] - S1 + s (its sequence's newest S1 positions are the S1
+// query tokens; negative positions are -1).
+template <bool kWindow>
 __device__ __forceinline__ void index_load(const Params& p, const Ctx& c, int j0, int lane, int (&idx)[8]) {
 #pragma unroll
   for (int k = 0; k < kIdxBatch; ++k) {
     const int jj = j0 + k;
     const int m = jj / p.n_tiles;
     const int e0 = (jj - m * p.n_tiles) * kTileKeys + lane;
-    const int32_t* tk = p.topk_idx + static_cast<int64_t>(token_of(p, c, m)) * p.topk;
+    const int t = token_of(p, c, m);
+    if constexpr (kWindow) {
+      const int b = t / p.S1;
+      const int first = (jj < c.total ? __ldg(p.act_seqs + b) : 0) - p.S1 + (t - b * p.S1) - p.window + 1;
 #pragma unroll
-    for (int u = 0; u < 2; ++u)
-      idx[2 * k + u] = (jj < c.total && e0 + 32 * u < p.topk) ? __ldg(tk + e0 + 32 * u) : -1;
+      for (int u = 0; u < 2; ++u) {
+        const int e = e0 + 32 * u;
+        idx[2 * k + u] = (jj < c.total && e < p.topk && first + e >= 0) ? first + e : -1;
+      }
+    } else {
+      const int32_t* tk = p.topk_idx + static_cast<int64_t>(t) * p.topk;
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+        idx[2 * k + u] = (jj < c.total && e0 + 32 * u < p.topk) ? __ldg(tk + e0 + 32 * u) : -1;
+    }
   }
 }
 
@@ -249,6 +265,7 @@ __device__ __forceinline__ void index_load(const Params& p, const Ctx& c, int j0
 // set-up barrier.  The stream runs through the cluster's tokens in order; a
 // pass may straddle two tokens, so each tile's sequence is found from its
 // position in the stream.
+template <bool kWindow>
 __device__ void index_role(const Params& p, const Ctx& c, int iw, int lane, int (&idx)[8]) {
   int32_t* rows = reinterpret_cast<int32_t*>(c.smem + kOffRows);
   // pull the cluster's top-k rows and their sequences' block-table rows towards
@@ -274,7 +291,7 @@ __device__ void index_role(const Params& p, const Ctx& c, int iw, int lane, int 
                    : -1;
     }
     int nxt[8];
-    index_load(p, c, j0 + kIndexWarps * kIdxBatch, lane, nxt);
+    index_load<kWindow>(p, c, j0 + kIndexWarps * kIdxBatch, lane, nxt);
     bool ok = true;
     for (int k = 0; k < nb && ok; ++k) {
       const int j = j0 + k;
@@ -783,7 +800,9 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
 }
 
 // ------------------------------------------------------------------ kernel
-template <bool kInt8>
+// kWindow: sliding-window positions instead of top-k lists (a separate
+// instantiation, so the top-k kernels compile exactly as without it).
+template <bool kInt8, bool kWindow>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_sparse_fwd_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -831,7 +850,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_spa
   // the index warps issue their first top-k loads before the set-up barrier
   int idx0[8];
   if (warp >= kIndexWarp && warp < kIndexWarp + kIndexWarps)
-    index_load(p, c, (warp - kIndexWarp) * kIdxBatch, lane, idx0);
+    index_load<kWindow>(p, c, (warp - kIndexWarp) * kIdxBatch, lane, idx0);
   if (warp == kMmaWarp) {
     tmem_alloc(c.sbase + kOffTmemSlot, kTmemCols);
     tmem_relinquish();
@@ -857,7 +876,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_spa
         if (lane == 0) mma_role(p, c);
         __syncwarp();
       } else if (warp < kIndexWarp + kIndexWarps) {
-        index_role(p, c, warp - kIndexWarp, lane, idx0);
+        index_role<kWindow>(p, c, warp - kIndexWarp, lane, idx0);
       }
     }
   }
@@ -891,22 +910,23 @@ mla_status fail(mla_status s, const char* fmt, ...) {
 bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0; }
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_attr_once[kMaxDevices][2];
-cudaError_t g_attr_err[kMaxDevices][2];
+std::once_flag g_attr_once[kMaxDevices][4];
+cudaError_t g_attr_err[kMaxDevices][4];
 
-int g_max_clusters[kMaxDevices][2];
+int g_max_clusters[kMaxDevices][4];
 
 // Also records how many two-CTA clusters of the kernel the device runs at once.
-template <bool kInt8>
+template <bool kInt8, bool kWindow>
 cudaError_t prepare_kernel(int dev) {
-  std::call_once(g_attr_once[dev][kInt8 ? 1 : 0], [dev] {
-    cudaError_t e = cudaFuncSetAttribute(mlasp::mla_sparse_fwd_kernel<kInt8>,
+  constexpr int kv = (kInt8 ? 1 : 0) + (kWindow ? 2 : 0);
+  std::call_once(g_attr_once[dev][kv], [dev] {
+    cudaError_t e = cudaFuncSetAttribute(mlasp::mla_sparse_fwd_kernel<kInt8, kWindow>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, mlasp::kSmemBytes);
     if (e == cudaSuccess) {
       // The warpgroups re-divide the registers the block is launched with;
       // refuse to launch if the compiled per-thread count cannot cover them.
       cudaFuncAttributes fa;
-      e = cudaFuncGetAttributes(&fa, mlasp::mla_sparse_fwd_kernel<kInt8>);
+      e = cudaFuncGetAttributes(&fa, mlasp::mla_sparse_fwd_kernel<kInt8, kWindow>);
       using R = mlasp::Regs<kInt8>;
       const long need = 256L * R::kSoftmax + 128L * 80 + 256L * R::kGather + 128L * R::kControl;
       if (e == cudaSuccess && (fa.numRegs < 80 || static_cast<long>(fa.numRegs) * mlasp::kThreads < need))
@@ -925,13 +945,13 @@ cudaError_t prepare_kernel(int dev) {
       cfg.attrs = attr;
       cfg.numAttrs = 1;
       int n = 0;
-      e = cudaOccupancyMaxActiveClusters(&n, mlasp::mla_sparse_fwd_kernel<kInt8>, &cfg);
-      g_max_clusters[dev][kInt8 ? 1 : 0] = n;
+      e = cudaOccupancyMaxActiveClusters(&n, mlasp::mla_sparse_fwd_kernel<kInt8, kWindow>, &cfg);
+      g_max_clusters[dev][kv] = n;
       if (e == cudaSuccess && n < 1) e = cudaErrorInvalidConfiguration;
     }
-    g_attr_err[dev][kInt8 ? 1 : 0] = e;
+    g_attr_err[dev][kv] = e;
   });
-  return g_attr_err[dev][kInt8 ? 1 : 0];
+  return g_attr_err[dev][kv];
 }
 
 }  // namespace
@@ -942,14 +962,22 @@ int32_t mla_sparse_abi_version(void) { return 100; }
 
 const char* mla_sparse_last_error(void) { return g_last_error; }
 
-mla_status mla_sparse_attn_fwd(const mla_dims* dims, const void* q_nope, const void* q_rope, const void* kv_nope,
-                               const void* kv_rope, const float* kv_scales, const int32_t* topk_idx,
-                               const int32_t* block_table, const int32_t* act_seqs, void* out, float* lse,
-                               float softmax_scale, int32_t mode, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared by both entry points: window == 0 reads the top-k lists, window > 0
+// builds each token's sliding window (d.topk is then the window).
+mla_status attn_fwd(const mla_dims* dims, const void* q_nope, const void* q_rope, const void* kv_nope,
+                    const void* kv_rope, const float* kv_scales, const int32_t* topk_idx, int32_t window,
+                    const int32_t* block_table, const int32_t* act_seqs, void* out, float* lse, float softmax_scale,
+                    int32_t mode, void* stream) {
   g_last_error[0] = '\0';
   if (dims == nullptr) return fail(MLA_ERR_NULL, "dims is NULL");
-  const mla_dims d = *dims;
-  if (!q_nope || !q_rope || !kv_nope || !kv_rope || !topk_idx || !block_table || !act_seqs || !out)
+  mla_dims d = *dims;
+  if (window < 0) return fail(MLA_ERR_SHAPE, "window=%d must be >= 1", window);
+  if (window > 0) d.topk = window;
+  if (!q_nope || !q_rope || !kv_nope || !kv_rope || (window == 0 && !topk_idx) || !block_table || !act_seqs || !out)
     return fail(MLA_ERR_NULL, "a required tensor pointer is NULL");
   if (d.kv_dtype != MLA_KV_BF16 && d.kv_dtype != MLA_KV_INT8)
     return fail(MLA_ERR_DTYPE, "kv_dtype %d is neither MLA_KV_BF16 nor MLA_KV_INT8", d.kv_dtype);
@@ -970,7 +998,7 @@ mla_status mla_sparse_attn_fwd(const mla_dims* dims, const void* q_nope, const v
   if (!aligned(q_nope, 16) || !aligned(q_rope, 16) || !aligned(kv_nope, 16) || !aligned(kv_rope, 16) ||
       !aligned(out, 16) || (kv_scales && d.kv_dtype == MLA_KV_INT8 && !aligned(kv_scales, 16)))
     return fail(MLA_ERR_ALIGN, "q/kv/out/scales pointers must be 16-byte aligned");
-  if (!aligned(topk_idx, 4) || !aligned(block_table, 4) || !aligned(act_seqs, 4) || (lse && !aligned(lse, 4)))
+  if ((topk_idx && !aligned(topk_idx, 4)) || !aligned(block_table, 4) || !aligned(act_seqs, 4) || (lse && !aligned(lse, 4)))
     return fail(MLA_ERR_ALIGN, "index tensors and lse must be 4-byte aligned");
 
   int dev = 0;
@@ -978,7 +1006,12 @@ mla_status mla_sparse_attn_fwd(const mla_dims* dims, const void* q_nope, const v
   if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return fail(MLA_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
   const bool int8 = d.kv_dtype == MLA_KV_INT8;
-  e = int8 ? prepare_kernel<true>(dev) : prepare_kernel<false>(dev);
+  const bool win = window > 0;
+  const int kv = (int8 ? 1 : 0) + (win ? 2 : 0);
+  e = kv == 0 ? prepare_kernel<false, false>(dev)
+      : kv == 1 ? prepare_kernel<true, false>(dev)
+      : kv == 2 ? prepare_kernel<false, true>(dev)
+                : prepare_kernel<true, true>(dev);
   if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "kernel set-up: %s", cudaGetErrorString(e));
 
   mlasp::Params p;
@@ -1001,18 +1034,47 @@ mla_status mla_sparse_attn_fwd(const mla_dims* dims, const void* q_nope, const v
   p.scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634);
   // persistent clusters: as many as run at once (never more than tokens); cluster
   // c takes tokens c, c + n_clusters, ... as one stream of key tiles
-  const int max_clusters = g_max_clusters[dev][int8 ? 1 : 0];
+  const int max_clusters = g_max_clusters[dev][kv];
   p.T = static_cast<int>(T);
   p.n_clusters = static_cast<int>(T < max_clusters ? T : max_clusters);
+  p.window = window;
   const dim3 grid(static_cast<unsigned>(2 * p.n_clusters));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (int8)
-    mlasp::mla_sparse_fwd_kernel<true><<<grid, mlasp::kThreads, mlasp::kSmemBytes, s>>>(p);
+  if (kv == 0)
+    mlasp::mla_sparse_fwd_kernel<false, false><<<grid, mlasp::kThreads, mlasp::kSmemBytes, s>>>(p);
+  else if (kv == 1)
+    mlasp::mla_sparse_fwd_kernel<true, false><<<grid, mlasp::kThreads, mlasp::kSmemBytes, s>>>(p);
+  else if (kv == 2)
+    mlasp::mla_sparse_fwd_kernel<false, true><<<grid, mlasp::kThreads, mlasp::kSmemBytes, s>>>(p);
   else
-    mlasp::mla_sparse_fwd_kernel<false><<<grid, mlasp::kThreads, mlasp::kSmemBytes, s>>>(p);
+    mlasp::mla_sparse_fwd_kernel<true, true><<<grid, mlasp::kThreads, mlasp::kSmemBytes, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
   return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mla_status mla_sparse_attn_fwd(const mla_dims* dims, const void* q_nope, const void* q_rope, const void* kv_nope,
+                               const void* kv_rope, const float* kv_scales, const int32_t* topk_idx,
+                               const int32_t* block_table, const int32_t* act_seqs, void* out, float* lse,
+                               float softmax_scale, int32_t mode, void* stream) {
+  return attn_fwd(dims, q_nope, q_rope, kv_nope, kv_rope, kv_scales, topk_idx, 0, block_table, act_seqs, out, lse,
+                  softmax_scale, mode, stream);
+}
+
+mla_status mla_swa_fwd(const mla_dims* dims, const void* q_nope, const void* q_rope, const void* kv_nope,
+                       const void* kv_rope, const float* kv_scales, const int32_t* block_table,
+                       const int32_t* act_seqs, int32_t window, void* out, float* lse, float softmax_scale,
+                       int32_t mode, void* stream) {
+  if (window < 1) {
+    g_last_error[0] = '\0';
+    return fail(MLA_ERR_SHAPE, "window=%d must be >= 1", window);
+  }
+  return attn_fwd(dims, q_nope, q_rope, kv_nope, kv_rope, kv_scales, nullptr, window, block_table, act_seqs, out,
+                  lse, softmax_scale, mode, stream);
 }
 
 mla_status mla_sparse_device_status(void* stream, uint32_t* flags, int32_t clear) {

@@ -23,7 +23,7 @@ def declared_functions():
     names = set()
     for h in HEADERS:
         text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
-        names |= set(re.findall(r"\b(mla_(?:sparse|indexer|cache)_\w+)\s*\(", text))
+        names |= set(re.findall(r"\b(mla_(?:sparse|indexer|cache|swa)_\w+)\s*\(", text))
     return sorted(names)
 
 
@@ -33,7 +33,7 @@ def test_header_declares_the_entry_points():
             "mla_sparse_abi_version", "mla_indexer_topk", "mla_indexer_workspace_bytes",
             "mla_indexer_device_status", "mla_indexer_last_error", "mla_indexer_scores",
             "mla_indexer_select", "mla_indexer_topk_noalloc", "mla_cache_write", "mla_cache_last_error",
-            "mla_cache_device_status"} <= set(names)
+            "mla_cache_device_status", "mla_swa_fwd"} <= set(names)
 
 
 def test_library_exports_every_declared_function(lib):
@@ -242,3 +242,13 @@ def test_cache_write_argument_errors_are_reported_before_launch(lib, case, expec
     assert st == expect, (case, st, lib.mla_cache_last_error())
     if expect != 0:
         assert lib.mla_cache_last_error()
+
+
+@pytest.mark.parametrize("window,expect", [(0, -2), (-3, -2)])
+def test_swa_rejects_a_window_below_one(lib, window, expect):
+    from mla_sparse_top_gb300.binding import MlaDims
+    d = MlaDims(B=2, S1=2, n_q=128, n_kv=1, d_nope=512, d_rope=64, block_size=128, num_blocks=8,
+                max_blocks_per_seq=4, topk=0, kv_dtype=0)
+    p = [ctypes.c_void_p(0x100000 * (i + 1)) for i in range(7)]
+    st = lib.mla_swa_fwd(ctypes.byref(d), *p, window, ctypes.c_void_p(0x900000), None, ctypes.c_float(0.04), 0, None)
+    assert st == expect and b"window" in lib.mla_sparse_last_error()

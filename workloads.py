@@ -165,6 +165,15 @@ def varlen_decode(seed: int = 3, B: int = 64) -> dict:
     return make_inputs(B=B, S1=2, n_q=128, act_seqs=act, topk=2048, seed=seed, name="varlen_decode")
 
 
+def swa_decode(seed: int = 10, B: int = 64, window: int = 128) -> dict:
+    """Sliding-window attention inputs: B=64 S1=2 H=128, act 8192 each, 4096
+    shuffled blocks, bf16; the window is a parameter (the pages give none).
+    The top-k list that make_inputs draws is not used by this workload."""
+    inp = make_inputs(B=B, S1=2, n_q=128, act_seqs=[8192] * B, topk=64, seed=seed, name="swa_decode")
+    inp["window"] = int(window)
+    return inp
+
+
 def prefill(seed: int = 4, B: int = 4, S1: int = 1024) -> dict:
     """B=4, S1=1024 tokens at positions 7168..8191 of act 8192, causal top-2048."""
     act = 8192
@@ -179,6 +188,7 @@ NAMED = {
     "int8_decode": int8_decode,
     "varlen_decode": varlen_decode,
     "prefill": prefill,
+    "swa_decode": swa_decode,
 }
 
 

@@ -308,7 +308,7 @@ idx_scores_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
 constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kRegChunks = 16;                       // scores of the first 8192 positions live in registers
-constexpr int kSelGroup = kRegChunks * kSelThreads;  // positions per round
+constexpr int kSelGroup = kRegChunks * kSelThreads;  // positions per segment
 constexpr int kBuckets = 2048;                       // value buckets of the first selection step
 constexpr int kListCap = 256;                        // threshold-bucket keys ranked directly
 
@@ -345,7 +345,7 @@ __device__ __forceinline__ int value_bucket(float v, float lo_half, float scale)
 }
 
 // One CTA per token.  Position j = g * 8192 + c * 512 + tid sits in chunk c of
-// round g; round 0 keeps its scores in registers, later rounds (sequences
+// segment g; segment 0 keeps its scores in registers, later segments (sequences
 // longer than 8192) reload theirs.  The selection keeps every key above a
 // threshold key T and the first k_rem keys equal to T, in position order:
 //   1. candidate count, min and max (block reduction); all candidates are
@@ -372,7 +372,7 @@ __global__ void __launch_bounds__(kSelThreads) idx_topk_kernel(const SelectParam
   // positions past the block table's width have no block: not candidates
   if (tid == 0 && static_cast<int64_t>(act) > p.ld) atomicOr(&g_idx_status, MLA_DEVICE_BAD_BLOCK);
   const int n = static_cast<int>(min(static_cast<int64_t>(max(act, 0)), p.ld));
-  const int rounds = (n + kSelGroup - 1) / kSelGroup;
+  const int segments = (n + kSelGroup - 1) / kSelGroup;
   const float* row = p.scores + static_cast<int64_t>(t) * p.ld;
   int32_t* out = p.topk_idx + static_cast<int64_t>(t) * p.topk;
   const uint32_t topk = static_cast<uint32_t>(p.topk);
@@ -398,7 +398,7 @@ __global__ void __launch_bounds__(kSelThreads) idx_topk_kernel(const SelectParam
   {
     uint32_t nc = 0;
     float lo = INFINITY, hi = -INFINITY;
-    for (int g = 0; g < rounds; ++g) {
+    for (int g = 0; g < segments; ++g) {
 #pragma unroll
       for (int c = 0; c < kRegChunks; ++c) {
         const float v = val_at(g, c);
@@ -441,7 +441,7 @@ __global__ void __launch_bounds__(kSelThreads) idx_topk_kernel(const SelectParam
     uint32_t m = n_cand;        // keys in play
     if (bucketed) {
       // ---- 2. bucket histogram, then the bucket of the topk-th largest
-      for (int g = 0; g < rounds; ++g) {
+      for (int g = 0; g < segments; ++g) {
 #pragma unroll
         for (int c = 0; c < kRegChunks; ++c) {
           const float v = val_at(g, c);
@@ -495,7 +495,7 @@ __global__ void __launch_bounds__(kSelThreads) idx_topk_kernel(const SelectParam
     }
     if (bucketed && m <= static_cast<uint32_t>(kListCap)) {
       // ---- 3a. rank the keys of bucket bsel directly
-      for (int g = 0; g < rounds; ++g) {
+      for (int g = 0; g < segments; ++g) {
 #pragma unroll
         for (int c = 0; c < kRegChunks; ++c) {
           const float v = val_at(g, c);
@@ -531,7 +531,7 @@ __global__ void __launch_bounds__(kSelThreads) idx_topk_kernel(const SelectParam
         const int shift = 24 - 8 * pass;
         const uint32_t hi_mask = pass == 0 ? 0u : (0xFFFFFFFFu << (shift + 8));
         uint32_t* h = hb + (pass & 1) * 256;
-        for (int g = 0; g < rounds; ++g) {
+        for (int g = 0; g < segments; ++g) {
 #pragma unroll
           for (int c = 0; c < kRegChunks; ++c) {
             const float v = val_at(g, c);
@@ -581,9 +581,9 @@ __global__ void __launch_bounds__(kSelThreads) idx_topk_kernel(const SelectParam
     }
   }
 
-  // ---- 4. compaction in position order, one round of 8192 positions at a time
+  // ---- 4. compaction in position order, one segment of 8192 positions at a time
   uint32_t sel_run = 0, eq_run = 0;
-  for (int g = 0; g < rounds; ++g) {
+  for (int g = 0; g < segments; ++g) {
 #pragma unroll
     for (int c = 0; c < kRegChunks; ++c) {
       const uint32_t key = score_key(val_at(g, c));
@@ -634,8 +634,8 @@ __global__ void __launch_bounds__(kSelThreads) idx_topk_kernel(const SelectParam
         sel_before += sel[e];
       }
       if (lane == 31) {
-        bcast[2] = incl2;  // selected in this round
-        bcast[3] = incl;   // equal keys in this round
+        bcast[2] = incl2;  // selected in this segment
+        bcast[3] = incl;   // equal keys in this segment
       }
     }
     __syncthreads();
@@ -652,7 +652,7 @@ __global__ void __launch_bounds__(kSelThreads) idx_topk_kernel(const SelectParam
     }
     sel_run += bcast[2];
     eq_run += bcast[3];
-    __syncthreads();  // cnt and bcast are rewritten by the next round
+    __syncthreads();  // cnt and bcast are rewritten by the next segment
   }
   for (int i = static_cast<int>(min(sel_run, topk)) + tid; i < p.topk; i += kSelThreads) out[i] = -1;
 }

@@ -1,5 +1,7 @@
 """TEST INFRASTRUCTURE ONLY: the fp64 CPU oracle for sparse MLA attention, for
-the Lightning Indexer's top-k selection and for the paged cache writer.
+the Lightning Indexer's top-k selection, for the paged cache writer, for
+sliding-window attention and (``oracle.compressed``, numpy) for compressed /
+sparse compressed attention.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
 leg may import this package.  The CUDA product path never imports it and the

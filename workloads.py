@@ -371,3 +371,63 @@ def cache_write_to_device(inp: dict, device="cuda") -> dict:
     return dict(k_nope=bf(inp["k_nope"]), k_rope=bf(inp["k_rope"]), cache_index=raw(inp["cache_index"]),
                 kv_nope=raw(inp["kv_nope"]) if int8 else bf(inp["kv_nope"]), kv_rope=bf(inp["kv_rope"]),
                 kv_scales=raw(inp["kv_scales"]) if int8 else None)
+
+
+# ------------------------------------------------------------------ compressed attention (CFA / SCFA)
+def make_compressed_inputs(*, B: int, S1: int, n_q: int, act_seqs, window: int, cmp_ratio: int, seed: int,
+                           cmp_topk: int | None = None, kv_int8: bool = False, name: str = "custom") -> dict:
+    """Original cache and query as make_inputs, plus a compressed cache: entry i
+    of sequence b exists for (i + 1) * cmp_ratio <= act_b, rows ~ N(0, 1) (bf16,
+    or INT8 with group scales), paged through its own shuffled block table.
+    With ``cmp_topk`` (SCFA) each token gets a list of cmp_topk distinct
+    compressed entries drawn from its visible ones (padded with -1); without
+    it (CFA) there is no list."""
+    base = make_inputs(B=B, S1=S1, n_q=n_q, act_seqs=act_seqs, topk=1, seed=seed, kv_int8=kv_int8, name=name)
+    g = torch.Generator().manual_seed(int(seed) + 77)
+    act = np.asarray(base["act_seqs"], dtype=np.int64)
+    n_cmp = act // cmp_ratio
+    nb = [max(1, (int(c) + BLOCK_SIZE - 1) // BLOCK_SIZE) for c in n_cmp]
+    cnb = int(sum(nb))
+    perm = torch.randperm(cnb, generator=g).numpy().astype(np.int32)
+    cbt = np.full((B, max(nb)), -1, dtype=np.int32)
+    o = 0
+    for b in range(B):
+        cbt[b, : nb[b]] = perm[o:o + nb[b]]
+        o += nb[b]
+    rows = cnb * BLOCK_SIZE
+    cmp_rope = _randn_bf16(g, (rows, D_ROPE))
+    if kv_int8:
+        q8, sc = quantize_int8_groups(torch.randn((rows, D_NOPE), generator=g))
+        cmp_nope, cmp_scales = q8, sc
+    else:
+        cmp_nope, cmp_scales = _randn_bf16(g, (rows, D_NOPE)), None
+    out = dict(base, cmp_nope=cmp_nope, cmp_rope=cmp_rope, cmp_scales=cmp_scales, cmp_block_table=cbt)
+    out["dims"] = dict(base["dims"], cmp_num_blocks=cnb, cmp_max_blocks_per_seq=int(cbt.shape[1]),
+                       window=int(window), cmp_ratio=int(cmp_ratio), cmp_topk=int(cmp_topk or 0))
+    if cmp_topk:
+        T = B * S1
+        lists = np.full((T, cmp_topk), -1, dtype=np.int32)
+        for t in range(T):
+            b, s = divmod(t, S1)
+            p = int(act[b]) - S1 + s
+            vis = max(0, (p + 1) // cmp_ratio)
+            k = min(cmp_topk, vis)
+            if k:
+                lists[t, :k] = torch.randperm(vis, generator=g)[:k].numpy()
+        out["cmp_idx"] = lists
+    return out
+
+
+def cfa_decode(seed: int = 11, B: int = 64) -> dict:
+    """CFA: B=64 S1=2 H=128, act 8192, window 128, compression ratio 128 (64 compressed entries)."""
+    return make_compressed_inputs(B=B, S1=2, n_q=128, act_seqs=[8192] * B, window=128, cmp_ratio=128, seed=seed,
+                                  name="cfa_decode")
+
+
+def scfa_decode(seed: int = 12, B: int = 64) -> dict:
+    """SCFA: B=64 S1=2 H=128, act 8192, window 128, ratio 4 (2048 compressed entries), 512 selected per token."""
+    return make_compressed_inputs(B=B, S1=2, n_q=128, act_seqs=[8192] * B, window=128, cmp_ratio=4, cmp_topk=512,
+                                  seed=seed, name="scfa_decode")
+
+
+COMPRESSED_NAMED = {"cfa_decode": cfa_decode, "scfa_decode": scfa_decode}

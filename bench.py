@@ -55,7 +55,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mtp_decode",
-                    choices=sorted(workloads.NAMED) + sorted(workloads.INDEXER_NAMED)
+                    choices=sorted(workloads.NAMED) + sorted(workloads.COMPRESSED_NAMED)
+                    + sorted(workloads.INDEXER_NAMED)
                     + sorted(workloads.CACHE_WRITE_NAMED))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
@@ -85,8 +86,40 @@ def valid_mask(inp):
     return (tk >= 0) & (tk < act)
 
 
+def compressed_counts(inp):
+    """CFA / SCFA accounting: per sequence the unique rows of both caches its
+    tokens attend to (the window and visibility rules of the compressed entry
+    point), times the row bytes, plus the per-call I/O; flops per attended
+    entry as for the sparse attention."""
+    d = inp["dims"]
+    S1, H, W, r = d["S1"], d["n_q"], d["window"], d["cmp_ratio"]
+    rb = row_bytes(inp)
+    uniq, n_entries = 0, 0
+    for b in range(d["B"]):
+        act = int(inp["act_seqs"][b])
+        ori, cmpset = set(), set()
+        for s in range(S1):
+            p = act - S1 + s
+            win = range(max(0, p - W + 1), p + 1)
+            ori.update(win)
+            if "cmp_idx" in inp:
+                vis = [int(i) for i in inp["cmp_idx"][b * S1 + s] if i >= 0 and (int(i) + 1) * r - 1 <= p]
+            else:
+                vis = list(range(0, max(0, (p + 1) // r)))
+            cmpset.update(vis)
+            n_entries += len(win) + len(vis)
+        uniq += len(ori) + len(cmpset)
+    T = d["B"] * S1
+    io = T * H * (512 + 64) * 2 + T * H * 512 * 2 + T * H * 4 + inp["block_table"].nbytes + inp["act_seqs"].nbytes \
+        + inp["cmp_block_table"].nbytes + (inp["cmp_idx"].nbytes if "cmp_idx" in inp else 0)
+    return dict(n_valid=n_entries, gathered_bytes=n_entries * rb, roofline_bytes=uniq * rb + io,
+                flops=2.0 * H * n_entries * (576 + 512))
+
+
 def algorithmic_counts(inp):
     """Method's own work: counts from the actual inputs."""
+    if "cmp_ratio" in inp["dims"]:
+        return compressed_counts(inp)
     if "window" in inp:
         inp = dict(inp, topk_idx=window_positions(inp).astype(np.int32),
                    dims=dict(inp["dims"], topk=int(inp["window"])))
@@ -143,7 +176,7 @@ def ncu_traffic(workload, kernel=KERNEL_NAME, source=KERNEL_SOURCE):
 
 SEEDS = {"tiny_decode": 0, "mtp_decode": 1, "int8_decode": 2, "varlen_decode": 3, "prefill": 4, "swa_decode": 10,
          "indexer_decode": 5, "indexer_tiny": 6, "indexer_varlen": 7, "cache_write_decode": 8,
-         "cache_write_prefill": 9}
+         "cache_write_prefill": 9, "cfa_decode": 11, "scfa_decode": 12}
 
 
 def rank_seed(workload: str, rank: int) -> int:
@@ -166,13 +199,24 @@ def reduce_max_over_ranks(values, device):
 SWA_METRIC = "sliding-window MLA attn µs/call, % HBM roofline (B64 S1=2, window 128)"
 
 
+CFA_METRIC = "compressed MLA attn (CFA: window 128 + ratio-128 entries) µs/call, % HBM roofline (B64 S1=2)"
+SCFA_METRIC = "sparse compressed MLA attn (SCFA: window 128 + 512 of the ratio-4 entries) µs/call, % HBM roofline (B64 S1=2)"
+
+
 def metric_of(inp):
+    if "cmp_ratio" in inp["dims"]:
+        return SCFA_METRIC if "cmp_idx" in inp else CFA_METRIC
     return SWA_METRIC if "window" in inp else METRIC
 
 
 def run_config(workload, d, world, window=None):
     """The ``config`` object of the JSON line (the same for both arms)."""
-    sel = f"window={window} (sliding)" if window else f"topk={d['topk']}"
+    if "cmp_ratio" in d:
+        window = d["window"]
+        sel = (f"window={window} + compressed ratio {d['cmp_ratio']}"
+               + (f" top-{d['cmp_topk']}" if d.get("cmp_topk") else " (all visible)"))
+    else:
+        sel = f"window={window} (sliding)" if window else f"topk={d['topk']}"
     cfg = {
         "workload": f"{workload}: B={d['B']} S1={d['S1']} N_Q={d['n_q']} {sel} "
                     f"{'int8' if d['kv_int8'] else 'bf16'} paged cache ({d['num_blocks']} blocks of 128)",
@@ -185,6 +229,8 @@ def run_config(workload, d, world, window=None):
     if window:
         cfg["window"] = window
         del cfg["topk"]
+    if "cmp_ratio" in d:
+        cfg.update(cmp_ratio=d["cmp_ratio"], cmp_topk=d.get("cmp_topk") or None)
     return cfg
 
 
@@ -271,6 +317,10 @@ def oracle_call(inp, tokens=None):
     """The oracle for this workload: the sliding-window oracle when it has a
     window, the sparse-attention oracle otherwise."""
     import oracle
+    if "cmp_ratio" in inp["dims"]:
+        import oracle.compressed as comp
+        d = inp["dims"]
+        return comp.forward(inp, d["window"], d["cmp_ratio"], cmp_idx=inp.get("cmp_idx"), tokens=tokens)
     if "window" in inp:
         return oracle.swa_forward(inp, inp["window"], tokens=tokens)
     return oracle.forward(inp, tokens=tokens)
@@ -333,7 +383,7 @@ def main():
     mla.load_library()
 
     # every rank draws its own batch (weak scaling)
-    gen = workloads.NAMED[args.workload]
+    gen = workloads.NAMED.get(args.workload) or workloads.COMPRESSED_NAMED[args.workload]
     inp = gen(seed=rank_seed(args.workload, rank))
     counts = algorithmic_counts(inp)
     dev = workloads.to_device(inp)
@@ -342,9 +392,27 @@ def main():
     mode = inp.get("mode", "decode")
 
     window = inp.get("window")
+    cd = inp["dims"] if "cmp_ratio" in inp["dims"] else None
+    if cd is not None:
+        def _bf(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+
+        def _raw(a):
+            return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+        dev.update(cmp_nope=_raw(inp["cmp_nope"]) if cd["kv_int8"] else _bf(inp["cmp_nope"]),
+                   cmp_rope=_bf(inp["cmp_rope"]), cmp_scales=_raw(inp.get("cmp_scales")),
+                   cmp_block_table=_raw(inp["cmp_block_table"]), cmp_idx=_raw(inp.get("cmp_idx")))
 
     def launch():
-        if window:
+        if cd is not None:
+            mla.mla_compressed_attn_fwd(dev["q_nope"], dev["q_rope"], dev["kv_nope"], dev["kv_rope"],
+                                        dev["kv_scales"], dev["block_table"], dev["cmp_nope"], dev["cmp_rope"],
+                                        dev["cmp_scales"], dev["cmp_block_table"], dev["act_seqs"], dev["out"],
+                                        dev["lse"], window=cd["window"], cmp_ratio=cd["cmp_ratio"],
+                                        cmp_idx=dev["cmp_idx"], softmax_scale=inp["softmax_scale"], mode=mode,
+                                        dims=dims, stream=stream)
+        elif window:
             mla.mla_swa_fwd(dev["q_nope"], dev["q_rope"], dev["kv_nope"], dev["kv_rope"], dev["kv_scales"],
                             dev["block_table"], dev["act_seqs"], dev["out"], dev["lse"], window=window,
                             softmax_scale=inp["softmax_scale"], mode=mode, dims=dims, stream=stream)
@@ -384,7 +452,12 @@ def main():
     status = mla.device_status(clear=True)
 
     # end-to-end through the C ABI with host buffers (pinned), copies inside the timed region
-    host_in = {k: dev[k].cpu().pin_memory() for k in ("q_nope", "q_rope", "topk_idx", "block_table", "act_seqs")}
+    per_call = ["q_nope", "q_rope", "block_table", "act_seqs"]
+    if cd is not None:
+        per_call += ["cmp_block_table"] + (["cmp_idx"] if dev.get("cmp_idx") is not None else [])
+    elif not window:
+        per_call.append("topk_idx")
+    host_in = {k: dev[k].cpu().pin_memory() for k in per_call}
     host_out = dev["out"].cpu().pin_memory()
     host_lse = dev["lse"].cpu().pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
@@ -894,7 +967,7 @@ def run_reference(args, world, rank):
         return
     import oracle
     oracle.build()
-    gen = workloads.NAMED[args.workload]
+    gen = workloads.NAMED.get(args.workload) or workloads.COMPRESSED_NAMED[args.workload]
     inp = gen()
     d = inp["dims"]
     T = d["B"] * d["S1"]

@@ -137,6 +137,40 @@ mla_status mla_swa_fwd(const mla_dims* dims, const void* q_nope, const void* q_r
                        const int32_t* act_seqs, int32_t window, void* out, float* lse, float softmax_scale,
                        int32_t mode, void* stream);
 
+/*
+ * mla_compressed_attn_fwd -- compressed and sparse compressed flash attention
+ * (CFA / SCFA, "NPU DeepSeek-V4 PyPTO fused-operator optimization", sections
+ * CFA, SCFA and Compressor): each query token attends, under one softmax, to
+ * its window of the original cache and to entries of a compressed cache.
+ *   token (b, s) sits at p = act_seqs[b] - S1 + s; original part: positions
+ *   [p - window + 1, p] that are >= 0 (as mla_swa_fwd);
+ *   compressed entry i (the Compressor's output for positions
+ *   [i*ratio, (i+1)*ratio)) is visible iff (i+1)*ratio - 1 <= p;
+ *   CFA (sparse_idx == NULL): every visible entry; SCFA: the visible entries
+ *   of sparse_idx[b*S1 + s, 0:topk] (logical entry ids; others masked).
+ * The compressed cache has the original cache's row layout and dtype
+ * (dims->kv_dtype; INT8 rows need scales), paged by its own block table.
+ * Arguments otherwise as mla_swa_fwd; dims->topk is ignored.  Rows of either
+ * cache must stay below 2^30 (num_blocks < 2^23).
+ */
+typedef struct mla_cmp_cache {
+  const void* nope;           /* [num_blocks*128, d_nope] bf16 | int8, 16-byte aligned */
+  const void* rope;           /* [num_blocks*128, d_rope] bf16, 16-byte aligned */
+  const float* scales;        /* [num_blocks*128, d_nope/128] for INT8, else NULL */
+  const int32_t* block_table; /* [B, max_blocks_per_seq] */
+  int32_t num_blocks;
+  int32_t max_blocks_per_seq;
+  int32_t ratio;              /* compress ratio r >= 1 */
+  const int32_t* sparse_idx;  /* NULL (CFA) or [B*S1, topk] int32 (SCFA) */
+  int32_t topk;               /* width of sparse_idx (SCFA), ignored for CFA */
+} mla_cmp_cache;
+
+mla_status mla_compressed_attn_fwd(const mla_dims* dims, const void* q_nope, const void* q_rope,
+                                   const void* kv_nope, const void* kv_rope, const float* kv_scales,
+                                   const int32_t* block_table, const mla_cmp_cache* cmp,
+                                   const int32_t* act_seqs, int32_t window, void* out, float* lse,
+                                   float softmax_scale, int32_t mode, void* stream);
+
 /* Description of the last error on this thread ("" after a success). */
 const char* mla_sparse_last_error(void);
 

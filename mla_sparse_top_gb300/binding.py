@@ -24,7 +24,7 @@ MLA_KV_INT8 = 1
 MLA_DEVICE_BAD_BLOCK = 0x1
 MLA_DEVICE_TIMEOUT = 0x2
 
-EXPORTED_SYMBOLS = ("mla_sparse_attn_fwd", "mla_swa_fwd", "mla_sparse_last_error", "mla_sparse_device_status",
+EXPORTED_SYMBOLS = ("mla_sparse_attn_fwd", "mla_swa_fwd", "mla_compressed_attn_fwd", "mla_sparse_last_error", "mla_sparse_device_status",
                     "mla_sparse_abi_version", "mla_indexer_workspace_bytes", "mla_indexer_topk",
                     "mla_indexer_scores", "mla_indexer_select", "mla_indexer_device_status",
                     "mla_indexer_last_error", "mla_indexer_topk_noalloc", "mla_cache_write",
@@ -35,6 +35,14 @@ class MlaDims(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int32) for name in (
         "B", "S1", "n_q", "n_kv", "d_nope", "d_rope", "block_size", "num_blocks", "max_blocks_per_seq",
         "topk", "kv_dtype")]
+
+
+class MlaCmpCache(ctypes.Structure):
+    """mla_cmp_cache: the compressed cache of mla_compressed_attn_fwd."""
+    _fields_ = [("nope", ctypes.c_void_p), ("rope", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("block_table", ctypes.c_void_p), ("num_blocks", ctypes.c_int32),
+                ("max_blocks_per_seq", ctypes.c_int32), ("ratio", ctypes.c_int32),
+                ("sparse_idx", ctypes.c_void_p), ("topk", ctypes.c_int32)]
 
 
 class IndexerDims(ctypes.Structure):
@@ -65,6 +73,10 @@ def load_library(path: str = LIB_PATH):
     lib.mla_swa_fwd.argtypes = [ctypes.POINTER(MlaDims)] + [vp] * 7 + [ctypes.c_int32, vp, vp, ctypes.c_float,
                                                                         ctypes.c_int32, vp]
     lib.mla_swa_fwd.restype = ctypes.c_int
+    lib.mla_compressed_attn_fwd.argtypes = [ctypes.POINTER(MlaDims)] + [vp] * 6 + [ctypes.POINTER(MlaCmpCache), vp,
+                                                                                   ctypes.c_int32, vp, vp,
+                                                                                   ctypes.c_float, ctypes.c_int32, vp]
+    lib.mla_compressed_attn_fwd.restype = ctypes.c_int
     lib.mla_sparse_last_error.argtypes = []
     lib.mla_sparse_last_error.restype = ctypes.c_char_p
     lib.mla_sparse_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int32]
@@ -175,6 +187,38 @@ def mla_swa_fwd(q_nope, q_rope, kv_nope, kv_rope, kv_scales, block_table, act_se
                          _ptr(kv_scales if kv_int8 else None), _ptr(block_table), _ptr(act_seqs),
                          ctypes.c_int32(int(window)), _ptr(out), _ptr(lse), ctypes.c_float(softmax_scale),
                          ctypes.c_int32(int(mode)), _stream_handle(stream))
+    _check(st)
+    return out, lse
+
+
+def mla_compressed_attn_fwd(q_nope, q_rope, kv_nope, kv_rope, kv_scales, block_table, cmp_nope, cmp_rope,
+                            cmp_scales, cmp_block_table, act_seqs, out, lse=None, *, window: int, cmp_ratio: int,
+                            cmp_idx=None, softmax_scale=None, mode: int | str = MLA_MODE_DECODE, S1: int = 1,
+                            stream=None, dims: MlaDims | None = None):
+    """Enqueue one call of the C entry point with the same name: each token's
+    window of the original cache plus the compressed cache's visible entries
+    (CFA, cmp_idx None) or the visible entries of cmp_idx (SCFA, (B*S1, K)
+    int32).  The compressed cache has the original layout and dtype."""
+    lib = load_library()
+    kv_int8 = kv_nope.dtype == torch.int8
+    if dims is None:
+        T, n_q, d_nope = q_nope.shape
+        dims = MlaDims(B=T // S1, S1=S1, n_q=n_q, n_kv=1, d_nope=d_nope, d_rope=64, block_size=128,
+                       num_blocks=kv_nope.shape[0] // 128, max_blocks_per_seq=block_table.shape[1], topk=window,
+                       kv_dtype=MLA_KV_INT8 if kv_int8 else MLA_KV_BF16)
+    if isinstance(mode, str):
+        mode = {"decode": MLA_MODE_DECODE, "prefill": MLA_MODE_PREFILL}[mode]
+    if softmax_scale is None:
+        softmax_scale = (dims.d_nope + dims.d_rope) ** -0.5
+    cmp = MlaCmpCache(nope=_ptr(cmp_nope), rope=_ptr(cmp_rope), scales=_ptr(cmp_scales if kv_int8 else None),
+                      block_table=_ptr(cmp_block_table), num_blocks=cmp_nope.shape[0] // 128,
+                      max_blocks_per_seq=cmp_block_table.shape[1], ratio=int(cmp_ratio), sparse_idx=_ptr(cmp_idx),
+                      topk=int(cmp_idx.shape[1]) if cmp_idx is not None else 0)
+    st = lib.mla_compressed_attn_fwd(ctypes.byref(dims), _ptr(q_nope), _ptr(q_rope), _ptr(kv_nope), _ptr(kv_rope),
+                                     _ptr(kv_scales if kv_int8 else None), _ptr(block_table), ctypes.byref(cmp),
+                                     _ptr(act_seqs), ctypes.c_int32(int(window)), _ptr(out), _ptr(lse),
+                                     ctypes.c_float(softmax_scale), ctypes.c_int32(int(mode)),
+                                     _stream_handle(stream))
     _check(st)
     return out, lse
 

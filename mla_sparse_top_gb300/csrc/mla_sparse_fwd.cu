@@ -52,6 +52,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "../../include/mla_sparse.h"
@@ -163,7 +164,14 @@ struct Params {
   int S1, n_q, topk, num_blocks, mbps, n_tiles;
   int T;           // query tokens B * S1
   int n_clusters;  // clusters in the grid; cluster c takes tokens c, c + n_clusters, ...
-  int window;      // > 0: sliding window of this many positions instead of top-k lists (topk = window)
+  int window;      // > 0: sliding window of this many positions instead of top-k lists
+  // compressed cache (mode 2): entries after the window are compressed entries
+  const void* cmp_nope;
+  const uint16_t* cmp_rope;
+  const float* cmp_scales;
+  const int32_t* cmp_block_table;
+  const int32_t* cmp_idx;  // SCFA lists [T, cmp_topk]; nullptr: CFA (every visible entry)
+  int cmp_num_blocks, cmp_mbps, cmp_ratio, cmp_topk;
   float scale_log2;
 };
 
@@ -231,12 +239,24 @@ __device__ __forceinline__ int seq_of_tile(const Params& p, const Ctx& c, int jj
   return token_of(p, c, jj / p.n_tiles) / p.S1;
 }
 
-// Entries (logical positions) of the pass starting at stream tile j0, -1
-// beyond the stream or the list: the token's top-k list, or with a sliding
-// window the positions p - window + 1 + e of the token at position
-// p = act_seqs[b] - S1 + s (its sequence's newest S1 positions are the S1
-// query tokens; negative positions are -1).
-template <bool kWindow>
+// Entry modes of the kernel: the token's top-k list (kModeLists), a sliding
+// window of positions (kModeWindow), or a window followed by compressed-cache
+// entries (kModeCompressed).  A compressed entry carries kCmpFlag through the
+// index and row rings.
+constexpr int kModeLists = 0;
+constexpr int kModeWindow = 1;
+constexpr int kModeCompressed = 2;
+constexpr int kCmpFlag = 1 << 30;
+
+// Entries of the pass starting at stream tile j0, -1 beyond the stream or the
+// list.  Lists: logical positions from topk_idx.  Window: the positions
+// p - window + 1 + e of the token at p = act_seqs[b] - S1 + s (its sequence's
+// newest S1 positions are the S1 query tokens; negative positions are -1).
+// Compressed: the window, then entry e' = e - window is compressed entry
+// e' (CFA) or cmp_idx[t, e'] (SCFA), kept when (i + 1) * cmp_ratio - 1 <= p:
+// entry i summarises positions [i * r, (i + 1) * r) and exists from the
+// position that completes it on.
+template <int kMode>
 __device__ __forceinline__ void index_load(const Params& p, const Ctx& c, int j0, int lane, int (&idx)[8]) {
 #pragma unroll
   for (int k = 0; k < kIdxBatch; ++k) {
@@ -244,13 +264,25 @@ __device__ __forceinline__ void index_load(const Params& p, const Ctx& c, int j0
     const int m = jj / p.n_tiles;
     const int e0 = (jj - m * p.n_tiles) * kTileKeys + lane;
     const int t = token_of(p, c, m);
-    if constexpr (kWindow) {
+    if constexpr (kMode != kModeLists) {
       const int b = t / p.S1;
-      const int first = (jj < c.total ? __ldg(p.act_seqs + b) : 0) - p.S1 + (t - b * p.S1) - p.window + 1;
+      const int pos = (jj < c.total ? __ldg(p.act_seqs + b) : 0) - p.S1 + (t - b * p.S1);
+      const int first = pos - p.window + 1;
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int e = e0 + 32 * u;
-        idx[2 * k + u] = (jj < c.total && e < p.topk && first + e >= 0) ? first + e : -1;
+        int v = -1;
+        if (jj < c.total && e < p.topk) {
+          if (e < p.window) {
+            v = first + e >= 0 ? first + e : -1;
+          } else if constexpr (kMode == kModeCompressed) {
+            const int e2 = e - p.window;
+            const int ci = p.cmp_idx != nullptr ? __ldg(p.cmp_idx + static_cast<int64_t>(t) * p.cmp_topk + e2) : e2;
+            v = (ci >= 0 && ci < (1 << 29) && static_cast<int64_t>(ci + 1) * p.cmp_ratio - 1 <= pos) ? (ci | kCmpFlag)
+                                                                                                   : -1;
+          }
+        }
+        idx[2 * k + u] = v;
       }
     } else {
       const int32_t* tk = p.topk_idx + static_cast<int64_t>(t) * p.topk;
@@ -265,16 +297,19 @@ __device__ __forceinline__ void index_load(const Params& p, const Ctx& c, int j0
 // set-up barrier.  The stream runs through the cluster's tokens in order; a
 // pass may straddle two tokens, so each tile's sequence is found from its
 // position in the stream.
-template <bool kWindow>
+template <int kMode>
 __device__ void index_role(const Params& p, const Ctx& c, int iw, int lane, int (&idx)[8]) {
   int32_t* rows = reinterpret_cast<int32_t*>(c.smem + kOffRows);
   // pull the cluster's top-k rows and their sequences' block-table rows towards
   // L2 up front (one 128-byte line per prefetch; the warps split the lines)
   for (int m = 0; m < c.ntok; ++m) {
     const int t = token_of(p, c, m);
-    const int32_t* tk = p.topk_idx + static_cast<int64_t>(t) * p.topk;
     const int32_t* bt = p.block_table + static_cast<int64_t>(t / p.S1) * p.mbps;
-    for (int e = (iw * 32 + lane) * 32; e < p.topk + 32; e += kIndexWarps * 32 * 32) prefetch_l2(tk + min(e, p.topk - 1));
+    if constexpr (kMode == kModeLists) {  // only list mode reads topk_idx
+      const int32_t* tk = p.topk_idx + static_cast<int64_t>(t) * p.topk;
+      for (int e = (iw * 32 + lane) * 32; e < p.topk + 32; e += kIndexWarps * 32 * 32)
+        prefetch_l2(tk + min(e, p.topk - 1));
+    }
     for (int e = (iw * 32 + lane) * 32; e < p.mbps + 32; e += kIndexWarps * 32 * 32) prefetch_l2(bt + min(e, p.mbps - 1));
   }
   bool bad = false;
@@ -285,13 +320,23 @@ __device__ void index_role(const Params& p, const Ctx& c, int iw, int lane, int 
     for (int q = 0; q < 8; ++q) {
       // the table entry is loaded for any index inside the table (without
       // waiting for the length check); entries outside [0, act) are dropped below
-      const int slot = idx[q] >> 7;
-      blk[q] = (idx[q] >= 0 && slot < p.mbps)
-                   ? __ldg(p.block_table + static_cast<int64_t>(seq_of_tile(p, c, j0 + (q >> 1))) * p.mbps + slot)
-                   : -1;
+      if constexpr (kMode == kModeCompressed) {
+        const bool cmp = idx[q] >= 0 && (idx[q] & kCmpFlag);
+        const int slot = (idx[q] & ~kCmpFlag) >> 7;
+        const int mb = cmp ? p.cmp_mbps : p.mbps;
+        const int32_t* bt = cmp ? p.cmp_block_table : p.block_table;
+        blk[q] = (idx[q] >= 0 && slot < mb)
+                     ? __ldg(bt + static_cast<int64_t>(seq_of_tile(p, c, j0 + (q >> 1))) * mb + slot)
+                     : -1;
+      } else {
+        const int slot = idx[q] >> 7;
+        blk[q] = (idx[q] >= 0 && slot < p.mbps)
+                     ? __ldg(p.block_table + static_cast<int64_t>(seq_of_tile(p, c, j0 + (q >> 1))) * p.mbps + slot)
+                     : -1;
+      }
     }
     int nxt[8];
-    index_load<kWindow>(p, c, j0 + kIndexWarps * kIdxBatch, lane, nxt);
+    index_load<kMode>(p, c, j0 + kIndexWarps * kIdxBatch, lane, nxt);
     bool ok = true;
     for (int k = 0; k < nb && ok; ++k) {
       const int j = j0 + k;
@@ -305,10 +350,12 @@ __device__ void index_role(const Params& p, const Ctx& c, int iw, int lane, int 
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int q = 2 * k + u;
-        const bool in_seq = idx[q] >= 0 && idx[q] < act;
-        const bool valid = in_seq && blk[q] >= 0 && blk[q] < p.num_blocks;
+        // a compressed entry was checked for visibility when it was loaded
+        const bool cmp = kMode == kModeCompressed && idx[q] >= 0 && (idx[q] & kCmpFlag);
+        const bool in_seq = idx[q] >= 0 && (cmp || idx[q] < act);
+        const bool valid = in_seq && blk[q] >= 0 && blk[q] < (cmp ? p.cmp_num_blocks : p.num_blocks);
         if (in_seq && !valid) bad = true;
-        const int row = blk[q] * 128 + (idx[q] & 127);
+        const int row = (blk[q] * 128 + (idx[q] & 127)) | (cmp ? kCmpFlag : 0);
         rows[((j0 + k) % kIdxSlots) * kTileKeys + u * 32 + lane] = valid ? row : -1;
       }
     }
@@ -339,13 +386,24 @@ __device__ __forceinline__ void dequant4(uint32_t w, float s, uint32_t& lo, uint
   hi = pack_bf16x2(f2, f3);
 }
 
-template <bool kInt8>
+// Row of the original or (mode 2, kCmpFlag) the compressed cache: base
+// pointer and row index for a valid ring entry.
+template <int kMode>
+__device__ __forceinline__ const uint8_t* row_base(const uint8_t* ori, const uint8_t* cmp, int32_t row, int64_t bytes) {
+  if constexpr (kMode == kModeCompressed) {
+    if (row & kCmpFlag) return cmp + static_cast<int64_t>(row & ~kCmpFlag) * bytes;
+  }
+  return ori + static_cast<int64_t>(row) * bytes;
+}
+
+template <bool kInt8, int kMode>
 __device__ void gather_role(const Params& p, const Ctx& c, int gw, int lane) {
   // all eight warps work on every tile; warp gw takes keys [8 gw, 8 gw + 8)
   const int key0 = gw * 8;
   const int32_t* rows_all = reinterpret_cast<const int32_t*>(c.smem + kOffRows);
   uint8_t* vmask8 = c.smem + kOffVmask;
   const uint8_t* kvr = reinterpret_cast<const uint8_t*>(p.kv_rope) + c.crank * 64 + (lane & 3) * 16;
+  const uint8_t* cmr = reinterpret_cast<const uint8_t*>(p.cmp_rope) + c.crank * 64 + (lane & 3) * 16;
   const int rk = key0 + (lane >> 2);  // rope: four 16-byte units per key, one per lane
   for (int j = 0; j < c.total; ++j) {
     const int st = j % kStages;
@@ -360,15 +418,16 @@ __device__ void gather_role(const Params& p, const Ctx& c, int gw, int lane) {
     if constexpr (!kInt8) {
       // latent half: 512 B per key, one key per warp instruction (32 lanes x 16 B)
       const uint8_t* kvn = reinterpret_cast<const uint8_t*>(p.kv_nope) + c.crank * 512 + lane * 16;
+      const uint8_t* cmn = reinterpret_cast<const uint8_t*>(p.cmp_nope) + c.crank * 512 + lane * 16;
       const uint32_t chunk = stage + (lane >> 3) * kChunkBytes;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int key = key0 + i;
         const int32_t row = rows[key];
         cp_async_16(chunk + key * 128 + (((lane & 7) ^ (key & 7)) << 4),
-                    row >= 0 ? kvn + static_cast<int64_t>(row) * 1024 : kvn, row >= 0 ? 16u : 0u);
+                    row >= 0 ? row_base<kMode>(kvn, cmn, row, 1024) : kvn, row >= 0 ? 16u : 0u);
       }
-      cp_async_16(rope + rope_unit(rk, lane & 3), rr >= 0 ? kvr + static_cast<int64_t>(rr) * 128 : kvr,
+      cp_async_16(rope + rope_unit(rk, lane & 3), rr >= 0 ? row_base<kMode>(kvr, cmr, rr, 128) : kvr,
                   rr >= 0 ? 16u : 0u);
       mbar_arrive_relaxed(c.bar(kBarIdxEmpty + slot));
       cp_async_arrive_noinc(c.bar(kBarFull + st));
@@ -380,17 +439,19 @@ __device__ void gather_role(const Params& p, const Ctx& c, int gw, int lane) {
       const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
       // latent half: 256 int8 per key = 16 lanes x 16 B; lanes 16-31 take the next key
       const int u = lane & 15;
-      const int8_t* kvn = reinterpret_cast<const int8_t*>(p.kv_nope) + c.crank * 256 + u * 16;
-      const float* scl = p.kv_scales + c.crank * 2 + (u >> 3);
+      const uint8_t* kvn = reinterpret_cast<const uint8_t*>(p.kv_nope) + c.crank * 256 + u * 16;
+      const uint8_t* cmn = reinterpret_cast<const uint8_t*>(p.cmp_nope) + c.crank * 256 + u * 16;
+      const uint8_t* scl = reinterpret_cast<const uint8_t*>(p.kv_scales + c.crank * 2 + (u >> 3));
+      const uint8_t* cms = reinterpret_cast<const uint8_t*>(p.cmp_scales + c.crank * 2 + (u >> 3));
       uint4 v[4];
       float sc[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int32_t row = rows[key0 + 2 * i + (lane >> 4)];
-        v[i] = row >= 0 ? ldg16(kvn + static_cast<int64_t>(row) * 512) : zero;
-        sc[i] = row >= 0 ? __ldg(scl + static_cast<int64_t>(row) * 4) : 0.f;
+        v[i] = row >= 0 ? ldg16(row_base<kMode>(kvn, cmn, row, 512)) : zero;
+        sc[i] = row >= 0 ? __ldg(reinterpret_cast<const float*>(row_base<kMode>(scl, cms, row, 16))) : 0.f;
       }
-      const uint4 qr = rr >= 0 ? ldg16(kvr + static_cast<int64_t>(rr) * 128) : zero;
+      const uint4 qr = rr >= 0 ? ldg16(row_base<kMode>(kvr, cmr, rr, 128)) : zero;
       mbar_arrive_relaxed(c.bar(kBarIdxEmpty + slot));
       const uint32_t chunk = stage + (u >> 2) * kChunkBytes;
       const int u8 = (u & 3) * 2;
@@ -800,9 +861,9 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
 }
 
 // ------------------------------------------------------------------ kernel
-// kWindow: sliding-window positions instead of top-k lists (a separate
-// instantiation, so the top-k kernels compile exactly as without it).
-template <bool kInt8, bool kWindow>
+// kMode: top-k lists, a sliding window, or a window plus compressed-cache
+// entries (separate instantiations, so each compiles only its own path).
+template <bool kInt8, int kMode>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_sparse_fwd_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -850,7 +911,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_spa
   // the index warps issue their first top-k loads before the set-up barrier
   int idx0[8];
   if (warp >= kIndexWarp && warp < kIndexWarp + kIndexWarps)
-    index_load<kWindow>(p, c, (warp - kIndexWarp) * kIdxBatch, lane, idx0);
+    index_load<kMode>(p, c, (warp - kIndexWarp) * kIdxBatch, lane, idx0);
   if (warp == kMmaWarp) {
     tmem_alloc(c.sbase + kOffTmemSlot, kTmemCols);
     tmem_relinquish();
@@ -868,7 +929,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_spa
     if (!*c.abort) sender_role(p, c, warp - kSenderWarp0, lane);
   } else if (warp < kMmaWarp) {
     regs_decrease<Regs<kInt8>::kGather>();
-    if (!*c.abort) gather_role<kInt8>(p, c, warp - kGatherWarp0, lane);
+    if (!*c.abort) gather_role<kInt8, kMode>(p, c, warp - kGatherWarp0, lane);
   } else {
     regs_decrease<Regs<kInt8>::kControl>();
     if (!*c.abort) {
@@ -876,7 +937,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_spa
         if (lane == 0) mma_role(p, c);
         __syncwarp();
       } else if (warp < kIndexWarp + kIndexWarps) {
-        index_role<kWindow>(p, c, warp - kIndexWarp, lane, idx0);
+        index_role<kMode>(p, c, warp - kIndexWarp, lane, idx0);
       }
     }
   }
@@ -910,23 +971,23 @@ mla_status fail(mla_status s, const char* fmt, ...) {
 bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0; }
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_attr_once[kMaxDevices][4];
-cudaError_t g_attr_err[kMaxDevices][4];
+std::once_flag g_attr_once[kMaxDevices][6];
+cudaError_t g_attr_err[kMaxDevices][6];
 
-int g_max_clusters[kMaxDevices][4];
+int g_max_clusters[kMaxDevices][6];
 
 // Also records how many two-CTA clusters of the kernel the device runs at once.
-template <bool kInt8, bool kWindow>
+template <bool kInt8, int kMode>
 cudaError_t prepare_kernel(int dev) {
-  constexpr int kv = (kInt8 ? 1 : 0) + (kWindow ? 2 : 0);
+  constexpr int kv = (kInt8 ? 1 : 0) + 2 * kMode;
   std::call_once(g_attr_once[dev][kv], [dev] {
-    cudaError_t e = cudaFuncSetAttribute(mlasp::mla_sparse_fwd_kernel<kInt8, kWindow>,
+    cudaError_t e = cudaFuncSetAttribute(mlasp::mla_sparse_fwd_kernel<kInt8, kMode>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, mlasp::kSmemBytes);
     if (e == cudaSuccess) {
       // The warpgroups re-divide the registers the block is launched with;
       // refuse to launch if the compiled per-thread count cannot cover them.
       cudaFuncAttributes fa;
-      e = cudaFuncGetAttributes(&fa, mlasp::mla_sparse_fwd_kernel<kInt8, kWindow>);
+      e = cudaFuncGetAttributes(&fa, mlasp::mla_sparse_fwd_kernel<kInt8, kMode>);
       using R = mlasp::Regs<kInt8>;
       const long need = 256L * R::kSoftmax + 128L * 80 + 256L * R::kGather + 128L * R::kControl;
       if (e == cudaSuccess && (fa.numRegs < 80 || static_cast<long>(fa.numRegs) * mlasp::kThreads < need))
@@ -945,7 +1006,7 @@ cudaError_t prepare_kernel(int dev) {
       cfg.attrs = attr;
       cfg.numAttrs = 1;
       int n = 0;
-      e = cudaOccupancyMaxActiveClusters(&n, mlasp::mla_sparse_fwd_kernel<kInt8, kWindow>, &cfg);
+      e = cudaOccupancyMaxActiveClusters(&n, mlasp::mla_sparse_fwd_kernel<kInt8, kMode>, &cfg);
       g_max_clusters[dev][kv] = n;
       if (e == cudaSuccess && n < 1) e = cudaErrorInvalidConfiguration;
     }
@@ -966,17 +1027,38 @@ const char* mla_sparse_last_error(void) { return g_last_error; }
 
 namespace {
 
-// Shared by both entry points: window == 0 reads the top-k lists, window > 0
-// builds each token's sliding window (d.topk is then the window).
+// Shared by the entry points: window == 0 reads the top-k lists, window > 0
+// builds each token's sliding window, followed by compressed-cache entries when
+// `cmp` is given (d.topk is then the number of entries per token).
 mla_status attn_fwd(const mla_dims* dims, const void* q_nope, const void* q_rope, const void* kv_nope,
                     const void* kv_rope, const float* kv_scales, const int32_t* topk_idx, int32_t window,
-                    const int32_t* block_table, const int32_t* act_seqs, void* out, float* lse, float softmax_scale,
-                    int32_t mode, void* stream) {
+                    const mla_cmp_cache* cmp, const int32_t* block_table, const int32_t* act_seqs, void* out,
+                    float* lse, float softmax_scale, int32_t mode, void* stream) {
   g_last_error[0] = '\0';
   if (dims == nullptr) return fail(MLA_ERR_NULL, "dims is NULL");
   mla_dims d = *dims;
   if (window < 0) return fail(MLA_ERR_SHAPE, "window=%d must be >= 1", window);
-  if (window > 0) d.topk = window;
+  int cmp_slots = 0;
+  if (cmp != nullptr) {
+    if (!cmp->nope || !cmp->rope || !cmp->block_table || (d.kv_dtype == MLA_KV_INT8 && !cmp->scales))
+      return fail(MLA_ERR_NULL, "a required compressed-cache pointer is NULL");
+    if (cmp->ratio < 1 || cmp->num_blocks < 1 || cmp->max_blocks_per_seq < 1 || (cmp->sparse_idx && cmp->topk < 1))
+      return fail(MLA_ERR_SHAPE, "compressed cache: ratio, num_blocks, max_blocks_per_seq (and topk for SCFA) must be >= 1");
+    if (cmp->num_blocks >= (1 << 23) || d.num_blocks >= (1 << 23))
+      return fail(MLA_ERR_SHAPE, "with a compressed cache both caches need num_blocks < 2^23");
+    if (!aligned(cmp->nope, 16) || !aligned(cmp->rope, 16) || (cmp->scales && !aligned(cmp->scales, 16)) ||
+        !aligned(cmp->block_table, 4) || (cmp->sparse_idx && !aligned(cmp->sparse_idx, 4)))
+      return fail(MLA_ERR_ALIGN, "compressed-cache rows must be 16-byte, tables 4-byte aligned");
+    // CFA: as many slots as the longest sequence can have compressed entries
+    const int64_t most = std::min<int64_t>(static_cast<int64_t>(cmp->max_blocks_per_seq) * 128,
+                                           static_cast<int64_t>(d.max_blocks_per_seq) * 128 / cmp->ratio);
+    cmp_slots = cmp->sparse_idx ? cmp->topk : static_cast<int>(most);
+  }
+  if (window > 0) {
+    if (static_cast<int64_t>(window) + cmp_slots > (1 << 24))
+      return fail(MLA_ERR_SHAPE, "window + compressed entries per token too large");
+    d.topk = window + cmp_slots;
+  }
   if (!q_nope || !q_rope || !kv_nope || !kv_rope || (window == 0 && !topk_idx) || !block_table || !act_seqs || !out)
     return fail(MLA_ERR_NULL, "a required tensor pointer is NULL");
   if (d.kv_dtype != MLA_KV_BF16 && d.kv_dtype != MLA_KV_INT8)
@@ -1006,12 +1088,16 @@ mla_status attn_fwd(const mla_dims* dims, const void* q_nope, const void* q_rope
   if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return fail(MLA_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
   const bool int8 = d.kv_dtype == MLA_KV_INT8;
-  const bool win = window > 0;
-  const int kv = (int8 ? 1 : 0) + (win ? 2 : 0);
-  e = kv == 0 ? prepare_kernel<false, false>(dev)
-      : kv == 1 ? prepare_kernel<true, false>(dev)
-      : kv == 2 ? prepare_kernel<false, true>(dev)
-                : prepare_kernel<true, true>(dev);
+  const int kmode = cmp != nullptr ? mlasp::kModeCompressed : (window > 0 ? mlasp::kModeWindow : mlasp::kModeLists);
+  const int kv = (int8 ? 1 : 0) + 2 * kmode;
+  switch (kv) {
+    case 0: e = prepare_kernel<false, mlasp::kModeLists>(dev); break;
+    case 1: e = prepare_kernel<true, mlasp::kModeLists>(dev); break;
+    case 2: e = prepare_kernel<false, mlasp::kModeWindow>(dev); break;
+    case 3: e = prepare_kernel<true, mlasp::kModeWindow>(dev); break;
+    case 4: e = prepare_kernel<false, mlasp::kModeCompressed>(dev); break;
+    default: e = prepare_kernel<true, mlasp::kModeCompressed>(dev); break;
+  }
   if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "kernel set-up: %s", cudaGetErrorString(e));
 
   mlasp::Params p;
@@ -1038,16 +1124,25 @@ mla_status attn_fwd(const mla_dims* dims, const void* q_nope, const void* q_rope
   p.T = static_cast<int>(T);
   p.n_clusters = static_cast<int>(T < max_clusters ? T : max_clusters);
   p.window = window;
+  p.cmp_nope = cmp ? cmp->nope : nullptr;
+  p.cmp_rope = cmp ? static_cast<const uint16_t*>(cmp->rope) : nullptr;
+  p.cmp_scales = cmp && int8 ? cmp->scales : nullptr;
+  p.cmp_block_table = cmp ? cmp->block_table : nullptr;
+  p.cmp_idx = cmp ? cmp->sparse_idx : nullptr;
+  p.cmp_num_blocks = cmp ? cmp->num_blocks : 0;
+  p.cmp_mbps = cmp ? cmp->max_blocks_per_seq : 0;
+  p.cmp_ratio = cmp ? cmp->ratio : 1;
+  p.cmp_topk = cmp_slots;
   const dim3 grid(static_cast<unsigned>(2 * p.n_clusters));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (kv == 0)
-    mlasp::mla_sparse_fwd_kernel<false, false><<<grid, mlasp::kThreads, mlasp::kSmemBytes, s>>>(p);
-  else if (kv == 1)
-    mlasp::mla_sparse_fwd_kernel<true, false><<<grid, mlasp::kThreads, mlasp::kSmemBytes, s>>>(p);
-  else if (kv == 2)
-    mlasp::mla_sparse_fwd_kernel<false, true><<<grid, mlasp::kThreads, mlasp::kSmemBytes, s>>>(p);
-  else
-    mlasp::mla_sparse_fwd_kernel<true, true><<<grid, mlasp::kThreads, mlasp::kSmemBytes, s>>>(p);
+  switch (kv) {
+    case 0: mlasp::mla_sparse_fwd_kernel<false, mlasp::kModeLists><<<grid, mlasp::kThreads, mlasp::kSmemBytes, s>>>(p); break;
+    case 1: mlasp::mla_sparse_fwd_kernel<true, mlasp::kModeLists><<<grid, mlasp::kThreads, mlasp::kSmemBytes, s>>>(p); break;
+    case 2: mlasp::mla_sparse_fwd_kernel<false, mlasp::kModeWindow><<<grid, mlasp::kThreads, mlasp::kSmemBytes, s>>>(p); break;
+    case 3: mlasp::mla_sparse_fwd_kernel<true, mlasp::kModeWindow><<<grid, mlasp::kThreads, mlasp::kSmemBytes, s>>>(p); break;
+    case 4: mlasp::mla_sparse_fwd_kernel<false, mlasp::kModeCompressed><<<grid, mlasp::kThreads, mlasp::kSmemBytes, s>>>(p); break;
+    default: mlasp::mla_sparse_fwd_kernel<true, mlasp::kModeCompressed><<<grid, mlasp::kThreads, mlasp::kSmemBytes, s>>>(p); break;
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
   return MLA_OK;
@@ -1061,8 +1156,8 @@ mla_status mla_sparse_attn_fwd(const mla_dims* dims, const void* q_nope, const v
                                const void* kv_rope, const float* kv_scales, const int32_t* topk_idx,
                                const int32_t* block_table, const int32_t* act_seqs, void* out, float* lse,
                                float softmax_scale, int32_t mode, void* stream) {
-  return attn_fwd(dims, q_nope, q_rope, kv_nope, kv_rope, kv_scales, topk_idx, 0, block_table, act_seqs, out, lse,
-                  softmax_scale, mode, stream);
+  return attn_fwd(dims, q_nope, q_rope, kv_nope, kv_rope, kv_scales, topk_idx, 0, nullptr, block_table, act_seqs, out,
+                  lse, softmax_scale, mode, stream);
 }
 
 mla_status mla_swa_fwd(const mla_dims* dims, const void* q_nope, const void* q_rope, const void* kv_nope,
@@ -1073,7 +1168,20 @@ mla_status mla_swa_fwd(const mla_dims* dims, const void* q_nope, const void* q_r
     g_last_error[0] = '\0';
     return fail(MLA_ERR_SHAPE, "window=%d must be >= 1", window);
   }
-  return attn_fwd(dims, q_nope, q_rope, kv_nope, kv_rope, kv_scales, nullptr, window, block_table, act_seqs, out,
+  return attn_fwd(dims, q_nope, q_rope, kv_nope, kv_rope, kv_scales, nullptr, window, nullptr, block_table, act_seqs,
+                  out, lse, softmax_scale, mode, stream);
+}
+
+mla_status mla_compressed_attn_fwd(const mla_dims* dims, const void* q_nope, const void* q_rope, const void* kv_nope,
+                                   const void* kv_rope, const float* kv_scales, const int32_t* block_table,
+                                   const mla_cmp_cache* cmp, const int32_t* act_seqs, int32_t window, void* out,
+                                   float* lse, float softmax_scale, int32_t mode, void* stream) {
+  if (window < 1 || cmp == nullptr) {
+    g_last_error[0] = '\0';
+    return fail(window < 1 ? MLA_ERR_SHAPE : MLA_ERR_NULL, window < 1 ? "window=%d must be >= 1" : "cmp is NULL (window %d)",
+                window);
+  }
+  return attn_fwd(dims, q_nope, q_rope, kv_nope, kv_rope, kv_scales, nullptr, window, cmp, block_table, act_seqs, out,
                   lse, softmax_scale, mode, stream);
 }
 

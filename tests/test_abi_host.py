@@ -23,7 +23,7 @@ def declared_functions():
     names = set()
     for h in HEADERS:
         text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
-        names |= set(re.findall(r"\b(mla_(?:sparse|indexer|cache|swa)_\w+)\s*\(", text))
+        names |= set(re.findall(r"\b(mla_(?:sparse|indexer|cache|swa|compressed)_\w+)\s*\(", text))
     return sorted(names)
 
 
@@ -33,7 +33,7 @@ def test_header_declares_the_entry_points():
             "mla_sparse_abi_version", "mla_indexer_topk", "mla_indexer_workspace_bytes",
             "mla_indexer_device_status", "mla_indexer_last_error", "mla_indexer_scores",
             "mla_indexer_select", "mla_indexer_topk_noalloc", "mla_cache_write", "mla_cache_last_error",
-            "mla_cache_device_status", "mla_swa_fwd"} <= set(names)
+            "mla_cache_device_status", "mla_swa_fwd", "mla_compressed_attn_fwd"} <= set(names)
 
 
 def test_library_exports_every_declared_function(lib):
@@ -252,3 +252,33 @@ def test_swa_rejects_a_window_below_one(lib, window, expect):
     p = [ctypes.c_void_p(0x100000 * (i + 1)) for i in range(7)]
     st = lib.mla_swa_fwd(ctypes.byref(d), *p, window, ctypes.c_void_p(0x900000), None, ctypes.c_float(0.04), 0, None)
     assert st == expect and b"window" in lib.mla_sparse_last_error()
+
+
+@pytest.mark.parametrize("case,expect", [("no_cmp", -1), ("window0", -2), ("ratio0", -2), ("scfa_topk0", -2),
+                                         ("int8_no_scales", -1), ("big_cache", -2), ("misaligned", -5)])
+def test_compressed_attn_argument_errors(lib, case, expect):
+    from mla_sparse_top_gb300.binding import MlaCmpCache, MlaDims
+    d = MlaDims(B=2, S1=2, n_q=128, n_kv=1, d_nope=512, d_rope=64, block_size=128, num_blocks=8,
+                max_blocks_per_seq=4, topk=0, kv_dtype=0)
+    P = lambda k: ctypes.c_void_p(0x100000 * k)
+    cmp = MlaCmpCache(nope=0x900000, rope=0xA00000, scales=None, block_table=0xB00000, num_blocks=2,
+                      max_blocks_per_seq=1, ratio=4, sparse_idx=None, topk=0)
+    window = 16
+    cref = ctypes.byref(cmp)
+    if case == "no_cmp":
+        cref = None
+    elif case == "window0":
+        window = 0
+    elif case == "ratio0":
+        cmp.ratio = 0
+    elif case == "scfa_topk0":
+        cmp.sparse_idx = 0xC00000
+    elif case == "int8_no_scales":
+        d.kv_dtype = 1
+    elif case == "big_cache":
+        cmp.num_blocks = 1 << 23
+    elif case == "misaligned":
+        cmp.nope = 0x900004
+    st = lib.mla_compressed_attn_fwd(ctypes.byref(d), P(1), P(2), P(3), P(4), P(5) if case == "int8_no_scales" else None,
+                                     P(6), cref, P(7), window, P(8), None, ctypes.c_float(0.04), 0, None)
+    assert st == expect, (case, st, lib.mla_sparse_last_error())

@@ -1,7 +1,8 @@
 """TEST INFRASTRUCTURE ONLY: the fp64 CPU oracle for sparse MLA attention, for
 the Lightning Indexer's top-k selection, for the paged cache writer, for
-sliding-window attention and (``oracle.compressed``, numpy) for compressed /
-sparse compressed attention.
+sliding-window attention, for compressed / sparse compressed attention
+(``oracle.compressed``, numpy) and for the MLA Prolog (``oracle.prolog``,
+numpy).
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
 leg may import this package.  The CUDA product path never imports it and the

@@ -431,3 +431,102 @@ def scfa_decode(seed: int = 12, B: int = 64) -> dict:
 
 
 COMPRESSED_NAMED = {"cfa_decode": cfa_decode, "scfa_decode": scfa_decode}
+
+
+# ------------------------------------------------------------------ MLA Prolog (synthetic weights)
+PROLOG_HIDDEN = 7168
+PROLOG_Q_LORA = 1536
+PROLOG_HEADS = 128
+PROLOG_QK_NOPE = 128
+PROLOG_KV = D_NOPE + D_ROPE
+
+
+def _randn_bf16_scaled(g: torch.Generator, shape, std: float, chunk_rows: int = 1 << 12) -> np.ndarray:
+    """N(0, std^2) rounded to bf16, drawn in row chunks."""
+    rows = shape[0]
+    out = np.empty(shape, dtype=np.uint16)
+    for r0 in range(0, rows, chunk_rows):
+        r1 = min(rows, r0 + chunk_rows)
+        out[r0:r1] = _bf16_bits(torch.randn((r1 - r0,) + tuple(shape[1:]), generator=g) * std)
+    return out
+
+
+def make_prolog_inputs(*, T: int, seed: int, hidden: int = PROLOG_HIDDEN, q_lora: int = PROLOG_Q_LORA,
+                       n_heads: int = PROLOG_HEADS, num_blocks: int = 4096, kv_int8: bool = True,
+                       skip_every: int = 0, name: str = "custom") -> dict:
+    """Hidden states, random-init weights and a paged cache for the MLA Prolog.
+
+    x (T, hidden) bf16 ~ N(0, 1), row 1 all zeros and row 2 scaled by 2^10 when
+    T >= 3; weights bf16 ~ N(0, 1/fan_in): wq_a (hidden, q_lora), wq_b
+    (q_lora, H*192), w_uk (H, 128, 512), wkv (hidden, 576); gamma_cq (q_lora,)
+    and gamma_ckv (576,) bf16 ~ U(0.5, 1.5); cos / sin (T, 32) fp32 of angles
+    ~ U(0, 2 pi); cache_index: distinct random flat rows (every
+    ``skip_every``-th -1); the existing cache holds random rows (bf16, or INT8
+    codes with scales).  No trained weights are involved."""
+    g = torch.Generator().manual_seed(int(seed))
+    H = int(n_heads)
+    xs = torch.randn((T, hidden), generator=g)
+    if T >= 3:
+        xs[1] = 0.0
+        xs[2] *= 2.0 ** 10
+    x = _bf16_bits(xs)
+    wq_a = _randn_bf16_scaled(g, (hidden, q_lora), hidden ** -0.5)
+    wq_b = _randn_bf16_scaled(g, (q_lora, H * (PROLOG_QK_NOPE + D_ROPE)), q_lora ** -0.5)
+    w_uk = _randn_bf16_scaled(g, (H, PROLOG_QK_NOPE, D_NOPE), PROLOG_QK_NOPE ** -0.5)
+    wkv = _randn_bf16_scaled(g, (hidden, PROLOG_KV), hidden ** -0.5)
+    gamma_cq = _bf16_bits(torch.empty(q_lora).uniform_(0.5, 1.5, generator=g))
+    gamma_ckv = _bf16_bits(torch.empty(PROLOG_KV).uniform_(0.5, 1.5, generator=g))
+    phi = torch.empty((T, D_ROPE // 2)).uniform_(0.0, 2.0 * math.pi, generator=g)
+    cos = torch.cos(phi).numpy().astype(np.float32)
+    sin = torch.sin(phi).numpy().astype(np.float32)
+    rows = num_blocks * BLOCK_SIZE
+    assert T <= rows
+    idx = torch.randperm(rows, generator=g)[:T].to(torch.int64).numpy()
+    if skip_every:
+        idx[::skip_every] = -1
+    kv_rope = _randn_bf16(g, (rows, D_ROPE))
+    if kv_int8:
+        kv_nope = torch.randint(-127, 128, (rows, D_NOPE), generator=g).to(torch.int8).numpy()
+        kv_scales = torch.empty((rows, 4)).uniform_(0.001, 0.1, generator=g).numpy().astype(np.float32)
+    else:
+        kv_nope = _randn_bf16(g, (rows, D_NOPE))
+        kv_scales = None
+    return dict(name=name, x=x, wq_a=wq_a, gamma_cq=gamma_cq, wq_b=wq_b, w_uk=w_uk, wkv=wkv, gamma_ckv=gamma_ckv,
+                cos=cos, sin=sin, cache_index=idx, kv_nope=kv_nope, kv_rope=kv_rope, kv_scales=kv_scales,
+                dims=dict(T=T, hidden=hidden, q_lora=q_lora, n_heads=H, num_blocks=num_blocks,
+                          kv_int8=int(bool(kv_int8))))
+
+
+def prolog_tiny(seed: int = 13) -> dict:
+    """13 tokens, hidden 256, q_lora 128, 4 heads, bf16 cache of 4 blocks, every 5th row skipped."""
+    return make_prolog_inputs(T=13, seed=seed, hidden=256, q_lora=128, n_heads=4, num_blocks=4, kv_int8=False,
+                              skip_every=5, name="prolog_tiny")
+
+
+def prolog_decode(seed: int = 14) -> dict:
+    """128 tokens (B=64 x S1=2 decode), DeepSeek-V3.2 sizes (hidden 7168, q_lora 1536, 128 heads),
+    INT8 cache of 4096 blocks."""
+    return make_prolog_inputs(T=128, seed=seed, num_blocks=4096, kv_int8=True, name="prolog_decode")
+
+
+def prolog_prefill(seed: int = 15) -> dict:
+    """1000 tokens (a ragged prefill chunk), DeepSeek-V3.2 sizes, bf16 cache of 4096 blocks."""
+    return make_prolog_inputs(T=1000, seed=seed, num_blocks=4096, kv_int8=False, name="prolog_prefill")
+
+
+PROLOG_NAMED = {"prolog_decode": prolog_decode, "prolog_prefill": prolog_prefill}
+
+
+def prolog_to_device(inp: dict, device="cuda") -> dict:
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+    def raw(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+    int8 = inp["dims"]["kv_int8"]
+    out = {k: bf(inp[k]) for k in ("x", "wq_a", "gamma_cq", "wq_b", "w_uk", "wkv", "gamma_ckv")}
+    out.update(cos=raw(inp["cos"]), sin=raw(inp["sin"]), cache_index=raw(inp["cache_index"]),
+               kv_nope=raw(inp["kv_nope"]) if int8 else bf(inp["kv_nope"]), kv_rope=bf(inp["kv_rope"]),
+               kv_scales=raw(inp["kv_scales"]) if int8 else None)
+    return out

@@ -13,6 +13,10 @@ per sequence, top-2048; one step = one mla_indexer_topk call (the score kernel, 
 selection kernel as a programmatic dependent launch).
 ``--workload cache_write_decode`` / ``cache_write_prefill`` time the paged
 cache writer (128 / 4096 new rows quantised into an INT8 cache of 4096 blocks).
+``--workload prolog_decode`` / ``prolog_prefill`` time the MLA Prolog (128 /
+1000 tokens, hidden 7168, q_lora 1536, 128 heads, random-init weights): one
+step = one mla_prolog call (four cuBLAS GEMMs and two of the library's
+kernels, the key projection on a forked stream).
 
 Prints one JSON line (rank 0).  ``value`` is microseconds per call (the
 device-timed kernel, CUDA events on the launching stream, L2 flushed by a
@@ -57,7 +61,7 @@ def parse_args():
     ap.add_argument("--workload", default="mtp_decode",
                     choices=sorted(workloads.NAMED) + sorted(workloads.COMPRESSED_NAMED)
                     + sorted(workloads.INDEXER_NAMED)
-                    + sorted(workloads.CACHE_WRITE_NAMED))
+                    + sorted(workloads.CACHE_WRITE_NAMED) + sorted(workloads.PROLOG_NAMED))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
     return ap.parse_args()
@@ -176,7 +180,7 @@ def ncu_traffic(workload, kernel=KERNEL_NAME, source=KERNEL_SOURCE):
 
 SEEDS = {"tiny_decode": 0, "mtp_decode": 1, "int8_decode": 2, "varlen_decode": 3, "prefill": 4, "swa_decode": 10,
          "indexer_decode": 5, "indexer_tiny": 6, "indexer_varlen": 7, "cache_write_decode": 8,
-         "cache_write_prefill": 9, "cfa_decode": 11, "scfa_decode": 12}
+         "cache_write_prefill": 9, "cfa_decode": 11, "scfa_decode": 12, "prolog_decode": 14, "prolog_prefill": 15}
 
 
 def rank_seed(workload: str, rank: int) -> int:
@@ -365,11 +369,15 @@ def main():
             return run_reference_indexer(args, world, rank)
         if args.workload in workloads.CACHE_WRITE_NAMED:
             return run_reference_cache_write(args, world, rank)
+        if args.workload in workloads.PROLOG_NAMED:
+            return run_reference_prolog(args, world, rank)
         return run_reference(args, world, rank)
     if args.workload in workloads.INDEXER_NAMED:
         return main_indexer(args, world, rank, local_rank)
     if args.workload in workloads.CACHE_WRITE_NAMED:
         return main_cache_write(args, world, rank, local_rank)
+    if args.workload in workloads.PROLOG_NAMED:
+        return main_prolog(args, world, rank, local_rank)
 
     import torch
     import torch.distributed as dist
@@ -956,6 +964,188 @@ def run_reference_cache_write(args, world, rank):
         "config": cache_write_config(args.workload, d, world),
         "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": "the whole call per step, writing in place"},
+        "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ MLA Prolog
+PROLOG_METRIC = "MLA Prolog µs/call (x -> absorbed q_nope/q_rope + cache row), % HBM roofline on weight bytes"
+
+
+def prolog_counts(inp):
+    """Algorithmic bytes and flops of one call: every weight, x, cos/sin and the
+    indices read once; q_nope, q_rope and the cache rows written once.  The
+    fp32 projections and bf16 operands kept in the workspace between launches
+    are not counted (a fused kernel would not need them)."""
+    d = inp["dims"]
+    T, hd, ql, H = d["T"], d["hidden"], d["q_lora"], d["n_heads"]
+    weights = 2 * (hd * ql + ql + ql * H * 192 + H * 128 * 512 + hd * 576 + 576)
+    n = int((inp["cache_index"] >= 0).sum())
+    rows = n * (((512 + 16) if d["kv_int8"] else 1024) + 128)
+    nbytes = weights + 2 * T * hd + 2 * 4 * T * 32 + 8 * T + 2 * T * H * (512 + 64) + rows
+    flops = 2 * T * (hd * ql + ql * H * 192 + H * 128 * 512 + hd * 576)
+    return nbytes, flops
+
+
+def prolog_config(workload, d, world):
+    return {
+        "workload": f"{workload}: T={d['T']} tokens, hidden {d['hidden']}, q_lora {d['q_lora']}, {d['n_heads']} heads "
+                    f"(DeepSeek-V3.2 sizes, random-init bf16 weights), {'INT8' if d['kv_int8'] else 'bf16'} paged "
+                    f"cache of {d['num_blocks']} blocks of 128",
+        "T": d["T"], "hidden": d["hidden"], "q_lora": d["q_lora"], "n_heads": d["n_heads"],
+        "kv_dtype": "int8" if d["kv_int8"] else "bf16",
+        "l2": "flushed between timed calls by a 256 MiB write (outside the per-call events)",
+        "launch": "a bounded GPU spin precedes each timed call, so its events time the device, not the host launch",
+        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+    }
+
+
+def main_prolog(args, world, rank, local_rank):
+    import torch
+    import torch.distributed as dist
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    import mla_sparse_top_gb300 as mla
+    from mla_sparse_top_gb300 import build
+    build.build()
+    mla.load_library()
+    inp = workloads.PROLOG_NAMED[args.workload](seed=rank_seed(args.workload, rank))
+    d = inp["dims"]
+    dev = workloads.prolog_to_device(inp)
+    T, H = d["T"], d["n_heads"]
+    q_nope = torch.empty((T, H, 512), dtype=torch.bfloat16, device="cuda")
+    q_rope = torch.empty((T, H, 64), dtype=torch.bfloat16, device="cuda")
+    dims = mla.prolog_dims(dev["x"], dev["wq_a"], dev["wq_b"], dev["kv_nope"])
+    ws = torch.empty(mla.mla_prolog_workspace_bytes(dims), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def launch():
+        mla.mla_prolog(dev["x"], dev["wq_a"], dev["gamma_cq"], dev["wq_b"], dev["w_uk"], dev["wkv"],
+                       dev["gamma_ckv"], dev["cos"], dev["sin"], dev["cache_index"], q_nope, q_rope, dev["kv_nope"],
+                       dev["kv_rope"], dev["kv_scales"], ws, dims=dims, stream=stream)
+
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    for i in range(max(3, args.warmup)):
+        flush.fill_(float(i))
+        launch()
+    torch.cuda.synchronize()
+    if mla.prolog_device_status(clear=True):
+        raise RuntimeError("prolog device status reported an error during warm-up")
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.15)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.mark_on()
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        spin_gpu()
+        starts[i].record(stream)
+        launch()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    clocks.mark_off()
+    if world > 1:
+        dist.barrier()
+    us = float(np.mean([a.elapsed_time(b) for a, b in zip(starts, ends)]) * 1000.0)
+    status = mla.prolog_device_status(clear=True)
+    # end to end: x, cos/sin and the indices from pinned host memory, the call, q_nope and q_rope back
+    host_in = {k: dev[k].cpu().pin_memory() for k in ("x", "cos", "sin", "cache_index")}
+    h_qn = torch.empty(q_nope.shape, dtype=q_nope.dtype, pin_memory=True)
+    h_qr = torch.empty(q_rope.shape, dtype=q_rope.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = h_qn.numel() * 2 + h_qr.numel() * 2
+    e2e_steps = max(5, min(args.steps, 50))
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    for i in range(e2e_steps + 2):
+        flush.fill_(float(i))
+        k = i - 2
+        if k >= 0:
+            e_s[k].record(stream)
+        for name, t in host_in.items():
+            dev[name].copy_(t, non_blocking=True)
+        launch()
+        h_qn.copy_(q_nope, non_blocking=True)
+        h_qr.copy_(q_rope, non_blocking=True)
+        if k >= 0:
+            e_e[k].record(stream)
+    torch.cuda.synchronize()
+    e2e_us = float(np.mean([a.elapsed_time(b) for a, b in zip(e_s, e_e)]) * 1000.0)
+    clock_summary = clocks.stop()
+    us, e2e_us = reduce_max_over_ranks([us, e2e_us], device="cuda")
+    if rank == 0:
+        hbm_gbs, bf16_tf, peak_src = measured_peaks()
+        nbytes, flops = prolog_counts(inp)
+        achieved = nbytes / (us * 1e-6) / 1e9
+        line = {
+            "metric": PROLOG_METRIC, "value": round(us, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(us / 1000.0, 6), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init weights)",
+            "config": prolog_config(args.workload, d, world),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_gbs, "unit": "GB/s",
+                         "frac": round(achieved / hbm_gbs, 4), "traffic": None,
+                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                         else "fallback",
+                         "algorithmic_bytes_per_launch": nbytes,
+                         "kernel": "the whole mla_prolog call (4 cuBLAS GEMMs + norm_rows_kernel + q_heads_kernel)",
+                         "tensor_tflops": round(flops / (us * 1e-6) / 1e12, 1),
+                         "tensor_frac_of_bf16_peak": round(flops / (us * 1e-6) / 1e12 / bf16_tf, 4)},
+            "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": int(d2h)},
+            "gpu_launches": 2 * args.steps, "library_launches": 4 * args.steps, "clocks": clock_summary,
+            "device_status": status,
+        }
+        if not args.no_cpu_baseline:
+            cus, sample = time_prolog_oracle(inp, min(args.cpu_seconds, 10.0))
+            line["cpu_baseline"] = {"value": round(cus, 1), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                                    "sample": sample}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def time_prolog_oracle(inp, target_s: float):
+    """The oracle (numpy fp64, its matrix products on numpy's BLAS threads) on
+    whole calls until ``target_s`` of CPU time is used."""
+    import oracle.prolog as P
+    reps, t_used = 0, 0.0
+    while t_used < target_s and reps < 100:
+        t0 = time.perf_counter()
+        P.forward_with_cache(inp)
+        t_used += time.perf_counter() - t0
+        reps += 1
+    return t_used / reps * 1e6, (f"the whole call, {reps} oracle calls ({t_used:.2f} s); numpy BLAS threads "
+                                 f"up to the host's cores")
+
+
+def run_reference_prolog(args, world, rank):
+    """The reference arm for a prolog workload: the oracle, as it stands, one whole call per step."""
+    if rank != 0:
+        return
+    inp = workloads.PROLOG_NAMED[args.workload]()
+    d = inp["dims"]
+    import oracle.prolog as P
+    for _ in range(min(args.warmup, 1)):
+        P.forward_with_cache(inp)
+    per_call = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        P.forward_with_cache(inp)
+        per_call.append((time.perf_counter() - t0) * 1e6)
+    us = float(np.mean(per_call))
+    line = {
+        "metric": PROLOG_METRIC, "value": round(us, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(us / 1000.0, 3), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (random-init weights)", "impl": "reference",
+        "config": prolog_config(args.workload, d, world),
+        "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": "the whole call per step (numpy BLAS threads up to the host's cores)"},
         "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

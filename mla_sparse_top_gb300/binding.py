@@ -1,4 +1,5 @@
-"""ctypes binding of the C ABI in include/mla_sparse.h and include/mla_indexer.h.
+"""ctypes binding of the C ABI in include/mla_sparse.h, mla_indexer.h,
+mla_cache.h and mla_prolog.h.
 
 Argument marshalling only: shapes and dtypes are read off torch tensors, the
 device pointers and the current CUDA stream are passed through, and a
@@ -28,7 +29,8 @@ EXPORTED_SYMBOLS = ("mla_sparse_attn_fwd", "mla_swa_fwd", "mla_compressed_attn_f
                     "mla_sparse_abi_version", "mla_indexer_workspace_bytes", "mla_indexer_topk",
                     "mla_indexer_scores", "mla_indexer_select", "mla_indexer_device_status",
                     "mla_indexer_last_error", "mla_indexer_topk_noalloc", "mla_cache_write",
-                    "mla_cache_last_error", "mla_cache_device_status")
+                    "mla_cache_last_error", "mla_cache_device_status", "mla_prolog_workspace_bytes", "mla_prolog",
+                    "mla_prolog_last_error", "mla_prolog_device_status")
 
 
 class MlaDims(ctypes.Structure):
@@ -48,6 +50,18 @@ class MlaCmpCache(ctypes.Structure):
 class IndexerDims(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int32) for name in (
         "B", "S1", "n_heads", "head_dim", "block_size", "num_blocks", "max_blocks_per_seq", "topk")]
+
+
+class PrologDims(ctypes.Structure):
+    """mla_prolog_dims."""
+    _fields_ = [("T", ctypes.c_int32), ("hidden", ctypes.c_int32), ("q_lora", ctypes.c_int32),
+                ("n_heads", ctypes.c_int32), ("num_rows", ctypes.c_int64), ("kv_int8", ctypes.c_int32),
+                ("eps", ctypes.c_float)]
+
+
+class PrologWeights(ctypes.Structure):
+    """mla_prolog_weights (device pointers)."""
+    _fields_ = [(name, ctypes.c_void_p) for name in ("wq_a", "gamma_cq", "wq_b", "w_uk", "wkv", "gamma_ckv")]
 
 
 class MlaError(RuntimeError):
@@ -103,6 +117,15 @@ def load_library(path: str = LIB_PATH):
     lib.mla_indexer_device_status.restype = ctypes.c_int
     lib.mla_indexer_last_error.argtypes = []
     lib.mla_indexer_last_error.restype = ctypes.c_char_p
+    lib.mla_prolog_workspace_bytes.argtypes = [ctypes.POINTER(PrologDims)]
+    lib.mla_prolog_workspace_bytes.restype = ctypes.c_size_t
+    lib.mla_prolog.argtypes = [ctypes.POINTER(PrologDims), vp, ctypes.POINTER(PrologWeights)] + [vp] * 9 + [
+        ctypes.c_size_t, vp]
+    lib.mla_prolog.restype = ctypes.c_int
+    lib.mla_prolog_last_error.argtypes = []
+    lib.mla_prolog_last_error.restype = ctypes.c_char_p
+    lib.mla_prolog_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int32]
+    lib.mla_prolog_device_status.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -331,4 +354,56 @@ def cache_device_status(clear: bool = True, stream=None) -> int:
     st = lib.mla_cache_device_status(_stream_handle(stream), ctypes.byref(flags), 1 if clear else 0)
     if st not in (MLA_OK, -7):
         raise MlaError(st, lib.mla_cache_last_error().decode())
+    return int(flags.value)
+
+
+# ------------------------------------------------------------------ MLA Prolog
+PROLOG_EPS = 1e-6
+
+
+def prolog_dims(x, wq_a, wq_b, kv_nope, eps: float = PROLOG_EPS) -> PrologDims:
+    """PrologDims read off the tensors: x (T, hidden), wq_a (hidden, q_lora),
+    wq_b (q_lora, H * 192), kv_nope (rows, 512)."""
+    return PrologDims(T=int(x.shape[0]), hidden=int(x.shape[1]), q_lora=int(wq_a.shape[1]),
+                      n_heads=int(wq_b.shape[1]) // 192, num_rows=int(kv_nope.shape[0]),
+                      kv_int8=1 if kv_nope.element_size() == 1 else 0, eps=float(eps))
+
+
+def mla_prolog_workspace_bytes(dims: PrologDims) -> int:
+    return int(load_library().mla_prolog_workspace_bytes(ctypes.byref(dims)))
+
+
+def mla_prolog(x, wq_a, gamma_cq, wq_b, w_uk, wkv, gamma_ckv, cos, sin, cache_index, q_nope, q_rope, kv_nope,
+               kv_rope, kv_scales, workspace, *, eps: float = PROLOG_EPS, dims: PrologDims | None = None,
+               stream=None):
+    """Enqueue one call of the C entry point with the same name.
+
+    x (T, hidden) bf16; weights bf16: wq_a (hidden, q_lora), gamma_cq (q_lora,),
+    wq_b (q_lora, H*192), w_uk (H, 128, 512), wkv (hidden, 576), gamma_ckv
+    (576,); cos / sin (T, 32) fp32; cache_index (T,) int64; outputs q_nope
+    (T, H, 512) and q_rope (T, H, 64) bf16; the cache kv_nope (rows, 512) bf16
+    or int8 (then kv_scales (rows, 4) fp32) and kv_rope (rows, 64) bf16 is
+    updated in place; workspace: a device tensor of at least
+    mla_prolog_workspace_bytes(dims) bytes."""
+    lib = load_library()
+    if dims is None:
+        dims = prolog_dims(x, wq_a, wq_b, kv_nope, eps)
+    wts = PrologWeights(wq_a=_ptr(wq_a), gamma_cq=_ptr(gamma_cq), wq_b=_ptr(wq_b), w_uk=_ptr(w_uk), wkv=_ptr(wkv),
+                        gamma_ckv=_ptr(gamma_ckv))
+    nbytes = workspace.numel() * workspace.element_size()
+    st = lib.mla_prolog(ctypes.byref(dims), _ptr(x), ctypes.byref(wts), _ptr(cos), _ptr(sin), _ptr(cache_index),
+                        _ptr(q_nope), _ptr(q_rope), _ptr(kv_nope), _ptr(kv_rope),
+                        _ptr(kv_scales if dims.kv_int8 else None), _ptr(workspace), ctypes.c_size_t(nbytes),
+                        _stream_handle(stream))
+    if st != MLA_OK:
+        raise MlaError(st, lib.mla_prolog_last_error().decode())
+    return q_nope, q_rope
+
+
+def prolog_device_status(clear: bool = True, stream=None) -> int:
+    lib = load_library()
+    flags = ctypes.c_uint32(0)
+    st = lib.mla_prolog_device_status(_stream_handle(stream), ctypes.byref(flags), 1 if clear else 0)
+    if st not in (MLA_OK, -7):
+        raise MlaError(st, lib.mla_prolog_last_error().decode())
     return int(flags.value)

@@ -109,7 +109,7 @@ def forward(inp: dict, round_intermediates: bool = True, eps: float = EPS) -> di
     q_rope = rope_interleaved(q[..., D_QK_NOPE:], cos[:, None, :], sin[:, None, :])
     q_nope_n = rnd(q[..., :D_QK_NOPE])
     w_uk = bf16_to_f64(inp["w_uk"])                                  # (H, 128, 512)
-    q_nope = np.einsum("thd,hdl->thl", q_nope_n, w_uk)
+    q_nope = np.matmul(q_nope_n.transpose(1, 0, 2), w_uk).transpose(1, 0, 2)   # head h: q[:, h] @ w_uk[h]
     # key: one projection, RMSNorm over the whole row, rope on its tail
     k = rms_norm(x @ bf16_to_f64(inp["wkv"]), bf16_to_f64(inp["gamma_ckv"]), eps)
     k_rope = rope_interleaved(k[:, D_LATENT:], cos, sin)

@@ -9,7 +9,7 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADERS = [os.path.join(ROOT, "include", "mla_sparse.h"), os.path.join(ROOT, "include", "mla_indexer.h"),
-           os.path.join(ROOT, "include", "mla_cache.h")]
+           os.path.join(ROOT, "include", "mla_cache.h"), os.path.join(ROOT, "include", "mla_prolog.h")]
 
 
 @pytest.fixture(scope="module")
@@ -23,7 +23,7 @@ def declared_functions():
     names = set()
     for h in HEADERS:
         text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
-        names |= set(re.findall(r"\b(mla_(?:sparse|indexer|cache|swa|compressed)_\w+)\s*\(", text))
+        names |= set(re.findall(r"\b(mla_(?:sparse|indexer|cache|swa|compressed|prolog)(?:_\w+)?)\s*\(", text))
     return sorted(names)
 
 
@@ -33,7 +33,8 @@ def test_header_declares_the_entry_points():
             "mla_sparse_abi_version", "mla_indexer_topk", "mla_indexer_workspace_bytes",
             "mla_indexer_device_status", "mla_indexer_last_error", "mla_indexer_scores",
             "mla_indexer_select", "mla_indexer_topk_noalloc", "mla_cache_write", "mla_cache_last_error",
-            "mla_cache_device_status", "mla_swa_fwd", "mla_compressed_attn_fwd"} <= set(names)
+            "mla_cache_device_status", "mla_swa_fwd", "mla_compressed_attn_fwd", "mla_prolog",
+            "mla_prolog_workspace_bytes", "mla_prolog_last_error", "mla_prolog_device_status"} <= set(names)
 
 
 def test_library_exports_every_declared_function(lib):
@@ -282,3 +283,54 @@ def test_compressed_attn_argument_errors(lib, case, expect):
     st = lib.mla_compressed_attn_fwd(ctypes.byref(d), P(1), P(2), P(3), P(4), P(5) if case == "int8_no_scales" else None,
                                      P(6), cref, P(7), window, P(8), None, ctypes.c_float(0.04), 0, None)
     assert st == expect, (case, st, lib.mla_sparse_last_error())
+
+
+@pytest.mark.parametrize("case,expect", [
+    ("null_dims", -1), ("hidden_7", -2), ("q_lora_0", -2), ("heads_0", -2), ("eps_0", -2), ("rows_0", -2),
+    ("int8_2", -2), ("null_x", -1), ("null_weight", -1), ("int8_no_scales", -1), ("misaligned_x", -5),
+    ("misaligned_gamma", -5), ("misaligned_ws", -5), ("small_ws", -2), ("empty", 0)])
+def test_prolog_argument_errors_are_reported_before_launch(lib, case, expect):
+    from mla_sparse_top_gb300.binding import PrologDims, PrologWeights
+    d = PrologDims(T=4, hidden=64, q_lora=32, n_heads=2, num_rows=256, kv_int8=1, eps=1e-6)
+    P = lambda k: ctypes.c_void_p(0x100000 * k)
+    wts = PrologWeights(wq_a=0x1100000, gamma_cq=0x1200000, wq_b=0x1300000, w_uk=0x1400000, wkv=0x1500000,
+                        gamma_ckv=0x1600000)
+    args = [P(1), None, P(2), P(3), P(4), P(5), P(6), P(7), P(8), P(9), P(10)]  # x w cos sin idx qn qr kvn kvr sc ws
+    ws_bytes = lib.mla_prolog_workspace_bytes(ctypes.byref(d))
+    assert ws_bytes > 0
+    dref = ctypes.byref(d)
+    if case == "null_dims":
+        dref = None
+    elif case == "hidden_7":
+        d.hidden = 7
+    elif case == "q_lora_0":
+        d.q_lora = 0
+    elif case == "heads_0":
+        d.n_heads = 0
+    elif case == "eps_0":
+        d.eps = 0.0
+    elif case == "rows_0":
+        d.num_rows = 0
+    elif case == "int8_2":
+        d.kv_int8 = 2
+    elif case == "null_x":
+        args[0] = None
+    elif case == "null_weight":
+        wts.w_uk = None
+    elif case == "int8_no_scales":
+        args[9] = None
+    elif case == "misaligned_x":
+        args[0] = ctypes.c_void_p(0x100008)
+    elif case == "misaligned_gamma":
+        wts.gamma_ckv = 0x1600002
+    elif case == "misaligned_ws":
+        args[10] = ctypes.c_void_p(0xA00080)
+    elif case == "small_ws":
+        ws_bytes -= 1
+    elif case == "empty":
+        d.T = 0
+        args = [None] * 11
+    st = lib.mla_prolog(dref, args[0], ctypes.byref(wts), *args[2:10], args[10], ctypes.c_size_t(ws_bytes), None)
+    assert st == expect, (case, st, lib.mla_prolog_last_error())
+    if expect != 0:
+        assert lib.mla_prolog_last_error()

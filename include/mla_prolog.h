@@ -33,8 +33,10 @@
  * asynchronous on `stream`, argument errors returned before any launch with
  * mla_prolog_last_error() describing them.  The products are cuBLAS GEMMs; the
  * norms, rotations and the cache write are this library's kernels.  The key
- * projection runs on an internal second stream that forks from and joins back
- * into `stream` through events, so the call is capturable into a CUDA graph.
+ * path (its projection, norm, rotation and cache write) runs on an internal
+ * second stream that forks from `stream` and joins back into it through
+ * events before the call's work on `stream` ends, so the call is capturable
+ * into a CUDA graph.
  * The first call on each device creates that stream, the events and a cuBLAS
  * handle: make it before any stream capture begins.  Calls are serialised by
  * a lock (one handle per device).
@@ -86,8 +88,9 @@ size_t mla_prolog_workspace_bytes(const mla_prolog_dims* dims);
  * kv_rope     bf16 [num_rows, 64], updated in place
  * kv_scales   fp32 [num_rows, 4] (INT8 only; NULL for bf16), updated in place
  * workspace   >= mla_prolog_workspace_bytes(dims) bytes, 256-byte aligned
- * Every pointer 16-byte aligned (cache_index 8-byte).  Six launches and two
- * event records; MLA_ERR_SHAPE when the workspace is too small.
+ * Every pointer 16-byte aligned (cache_index 8-byte).  Seven launches (the
+ * key projection and the key-row kernel on the internal second stream) and
+ * two event records; MLA_ERR_SHAPE when the workspace is too small.
  */
 mla_status mla_prolog(const mla_prolog_dims* dims, const void* x, const mla_prolog_weights* w, const float* cos,
                       const float* sin, const int64_t* cache_index, void* q_nope, void* q_rope, void* kv_nope,

@@ -8,20 +8,23 @@
 // section MLA Prolog (weight absorption in decode: the query's no-position
 // part is taken into the 512-wide latent space by w_uk).
 //
-// Data flow per call (T tokens, H heads), six launches:
+// Data flow per call (T tokens, H heads), seven launches:
 //   side stream   kv_raw = x @ wkv                     cuBLAS, fp32 out
+//   side stream   kv_rows_kernel: k = RMSNorm(kv_raw) * gamma_ckv, RoPE on
+//                 k[512:], rounded to bf16 and written (bf16 or INT8) into
+//                 the cache row
 //   stream        c_raw  = x @ wq_a                    cuBLAS, fp32 out
-//   stream        norm_rows_kernel: c^Q = bf16(RMSNorm(c_raw) * gamma_cq) and
-//                 k = RMSNorm(kv_raw) * gamma_ckv, RoPE on k[512:], rounded to
-//                 bf16 and written (bf16 or INT8) into the cache row
+//   stream        cq_rows_kernel: c^Q = bf16(RMSNorm(c_raw) * gamma_cq)
 //   stream        q_raw  = c^Q @ wq_b                  cuBLAS, fp32 out
 //   stream        q_heads_kernel: per (t, h) RMSNorm over 192, q[:128] -> bf16
 //                 operand, RoPE(q[128:]) -> q_rope
 //   stream        q_nope[h] = q[h][:128] @ w_uk[h]     cuBLAS strided batched, bf16 out
-// The two projections of x are independent (the page runs them side by side
-// because neither fills the machine in decode); here they run on two streams.
-// The norms are memory-bound row passes: one warp per row, fp32 throughout,
-// one rounding to bf16 at each storage point.
+//   stream        waits for the side stream
+// The query and key paths are independent after x (the page runs the two
+// projections side by side because neither fills the machine in decode);
+// here they run on two streams.  The norms are memory-bound row passes in
+// fp32 with one rounding to bf16 at each storage point: a 128-thread block
+// per c^Q row, a warp per key row and per (token, head).
 #include <cublas_v2.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -102,32 +105,41 @@ __device__ __forceinline__ uint32_t code8(float x, float scale) {
   return static_cast<uint32_t>(static_cast<uint8_t>(static_cast<int8_t>(max(-128, min(127, q)))));
 }
 
-// Warps [0, T): the c^Q rows; warps [T, 2T): the key rows and their cache write.
-__global__ void __launch_bounds__(kWarps * 32) norm_rows_kernel(const NormParams p) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = blockIdx.x * kWarps + warp;
-  if (g < p.T) {
-    const int t = g;
-    const float4* src = reinterpret_cast<const float4*>(p.c_raw + static_cast<int64_t>(t) * p.q_lora);
-    const int n4 = p.q_lora >> 2;
-    float ss = 0.f;
-    for (int i = lane; i < n4; i += 32) {
-      const float4 v = src[i];
-      ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-    }
-    const float inv = inv_rms(warp_sum(ss), p.q_lora, p.eps);
-    const uint2* gam = reinterpret_cast<const uint2*>(p.gamma_cq);
-    uint2* dst = reinterpret_cast<uint2*>(p.c_q + static_cast<int64_t>(t) * p.q_lora);
-    for (int i = lane; i < n4; i += 32) {
-      const float4 v = src[i];
-      const uint2 gw = __ldg(gam + i);
-      dst[i] = make_uint2(pack_bf16(v.x * inv * bf16_lo(gw.x), v.y * inv * bf16_hi(gw.x)),
-                          pack_bf16(v.z * inv * bf16_lo(gw.y), v.w * inv * bf16_hi(gw.y)));
-    }
-    return;
+constexpr int kCqThreads = 128;
+
+// One block per c^Q row: sum of squares over the row, then the scaled, rounded row.
+__global__ void __launch_bounds__(kCqThreads) cq_rows_kernel(const NormParams p) {
+  __shared__ float part[kCqThreads / 32];
+  const int t = blockIdx.x;
+  const float4* src = reinterpret_cast<const float4*>(p.c_raw + static_cast<int64_t>(t) * p.q_lora);
+  const int n4 = p.q_lora >> 2;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < n4; i += kCqThreads) {
+    const float4 v = src[i];
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
   }
-  if (g >= 2 * p.T) return;
-  const int t = g - p.T;
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < kCqThreads / 32; ++w) tot += part[w];
+  const float inv = inv_rms(tot, p.q_lora, p.eps);
+  const uint2* gam = reinterpret_cast<const uint2*>(p.gamma_cq);
+  uint2* dst = reinterpret_cast<uint2*>(p.c_q + static_cast<int64_t>(t) * p.q_lora);
+  for (int i = threadIdx.x; i < n4; i += kCqThreads) {
+    const float4 v = src[i];
+    const uint2 gw = __ldg(gam + i);
+    dst[i] = make_uint2(pack_bf16(v.x * inv * bf16_lo(gw.x), v.y * inv * bf16_hi(gw.x)),
+                        pack_bf16(v.z * inv * bf16_lo(gw.y), v.w * inv * bf16_hi(gw.y)));
+  }
+}
+
+// One warp per key row: RMSNorm over the 576-wide row, RoPE on its tail, the cache write.
+__global__ void __launch_bounds__(kWarps * 32) kv_rows_kernel(const NormParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kWarps + warp;
+  if (t >= p.T) return;
   // lane l: latent dims [16 l, 16 l + 16) (eight lanes per 128-element group) and rope pair l
   const float* row = p.kv_raw + static_cast<int64_t>(t) * kKv;
   float x[16];
@@ -363,21 +375,6 @@ mla_status mla_prolog(const mla_prolog_dims* dims, const void* x, const mla_prol
   float* q_raw = reinterpret_cast<float*>(ws + L.q_raw);
   uint16_t* q_n = reinterpret_cast<uint16_t*>(ws + L.q_n);
 
-  // key projection on the side stream, forked from and joined back into `s`
-  PRO_CUDA(cudaEventRecord(st.fork, s), "recording the fork event");
-  PRO_CUDA(cudaStreamWaitEvent(st.side, st.fork, 0), "side stream wait");
-  PRO_BLAS(cublasSetStream(st.blas, st.side), "cublasSetStream");
-  PRO_BLAS(cublasSetWorkspace(st.blas, ws + L.ws_side, kBlasWsSide), "cublasSetWorkspace");
-  mla_status gs = gemm_rm(st.blas, T, kKv, hidden, x, hidden, w->wkv, kKv, kv_raw, kKv, CUDA_R_32F, "x @ wkv");
-  if (gs != MLA_OK) return gs;
-  PRO_CUDA(cudaEventRecord(st.join, st.side), "recording the join event");
-
-  PRO_BLAS(cublasSetStream(st.blas, s), "cublasSetStream");
-  PRO_BLAS(cublasSetWorkspace(st.blas, ws + L.ws_main, kBlasWsMain), "cublasSetWorkspace");
-  gs = gemm_rm(st.blas, T, q_lora, hidden, x, hidden, w->wq_a, q_lora, c_raw, q_lora, CUDA_R_32F, "x @ wq_a");
-  if (gs != MLA_OK) return gs;
-  PRO_CUDA(cudaStreamWaitEvent(s, st.join, 0), "join wait");
-
   NormParams np;
   np.c_raw = c_raw;
   np.gamma_cq = static_cast<const uint16_t*>(w->gamma_cq);
@@ -395,8 +392,25 @@ mla_status mla_prolog(const mla_prolog_dims* dims, const void* x, const mla_prol
   np.T = T;
   np.int8 = dims->kv_int8;
   np.eps = dims->eps;
-  norm_rows_kernel<<<static_cast<unsigned>((2 * T + kWarps - 1) / kWarps), kWarps * 32, 0, s>>>(np);
-  PRO_CUDA(cudaGetLastError(), "norm_rows_kernel launch");
+
+  // key path on the side stream, forked from `s` here and joined back at the end
+  PRO_CUDA(cudaEventRecord(st.fork, s), "recording the fork event");
+  PRO_CUDA(cudaStreamWaitEvent(st.side, st.fork, 0), "side stream wait");
+  PRO_BLAS(cublasSetStream(st.blas, st.side), "cublasSetStream");
+  PRO_BLAS(cublasSetWorkspace(st.blas, ws + L.ws_side, kBlasWsSide), "cublasSetWorkspace");
+  mla_status gs = gemm_rm(st.blas, T, kKv, hidden, x, hidden, w->wkv, kKv, kv_raw, kKv, CUDA_R_32F, "x @ wkv");
+  if (gs != MLA_OK) return gs;
+  kv_rows_kernel<<<static_cast<unsigned>((T + kWarps - 1) / kWarps), kWarps * 32, 0, st.side>>>(np);
+  PRO_CUDA(cudaGetLastError(), "kv_rows_kernel launch");
+  PRO_CUDA(cudaEventRecord(st.join, st.side), "recording the join event");
+
+  // query path on `s`
+  PRO_BLAS(cublasSetStream(st.blas, s), "cublasSetStream");
+  PRO_BLAS(cublasSetWorkspace(st.blas, ws + L.ws_main, kBlasWsMain), "cublasSetWorkspace");
+  gs = gemm_rm(st.blas, T, q_lora, hidden, x, hidden, w->wq_a, q_lora, c_raw, q_lora, CUDA_R_32F, "x @ wq_a");
+  if (gs != MLA_OK) return gs;
+  cq_rows_kernel<<<static_cast<unsigned>(T), kCqThreads, 0, s>>>(np);
+  PRO_CUDA(cudaGetLastError(), "cq_rows_kernel launch");
 
   gs = gemm_rm(st.blas, T, H * kQHead, q_lora, c_q, q_lora, w->wq_b, H * kQHead, q_raw, H * kQHead, CUDA_R_32F,
                "c^Q @ wq_b");
@@ -421,6 +435,7 @@ mla_status mla_prolog(const mla_prolog_dims* dims, const void* x, const mla_prol
                                       CUDA_R_16BF, H * kQkNope, kQkNope, &zero, q_nope, CUDA_R_16BF, H * kLatent,
                                       kLatent, H, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT),
            "absorption q_nope @ w_uk");
+  PRO_CUDA(cudaStreamWaitEvent(s, st.join, 0), "join wait");
   return MLA_OK;
 }
 

@@ -13,7 +13,7 @@ KEYS = {"metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "
         "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"}
 
 
-@pytest.mark.parametrize("workload", ["tiny_decode", "indexer_tiny", "cache_write_decode"])
+@pytest.mark.parametrize("workload", ["tiny_decode", "indexer_tiny", "cache_write_decode", "prolog_decode"])
 def test_reference_arm_prints_one_contract_line(workload):
     r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", workload, "--steps", "1",
                         "--warmup", "0"], cwd=ROOT, capture_output=True, text=True, timeout=300)

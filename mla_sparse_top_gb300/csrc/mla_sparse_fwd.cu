@@ -81,7 +81,7 @@ struct Regs {
 };
 
 constexpr int kTileKeys = 64;
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kRegions = 3;  // TMEM score/P regions: tiles i, i+1, i+2 in flight
 constexpr int kIdxSlots = kIndexWarps * kIdxBatch;
 constexpr int kHeads = 128;
@@ -93,8 +93,8 @@ constexpr int kXchgBlockBytes = 32 * 32 * 4;           // its 32 heads of one TM
 constexpr int kQHalfBytes = kHeads * 128 * 2;          // Q latent dims [128, 256) of this CTA (bf16)
 constexpr int kQRopeBytes = kHeads * 64;
 
-constexpr int kOffRecv = 0;                            // same offset in both CTAs (peer writes here)
-constexpr int kOffStaging = kOffRecv + kXchgBytes;
+constexpr int kOffRecv = 0;                            // [2] one slot per column half, same offset in both CTAs
+constexpr int kOffStaging = kOffRecv + 2 * kXchgBytes;
 constexpr int kOffStages = kOffStaging + kXchgBytes;
 constexpr int kOffQHalf = kOffStages + kStages * kStageBytes;
 constexpr int kOffQRope = kOffQHalf + kQHalfBytes;
@@ -111,11 +111,12 @@ constexpr int kBarSFull = kBarIdxEmpty + kIdxSlots;      // [kRegions] S(i) comp
 constexpr int kBarSFree = kBarSFull + kRegions;          // [kRegions] senders have read S(i)
 constexpr int kBarPFull = kBarSFree + kRegions;          // [kRegions] P(i) written
 constexpr int kBarPvDone = kBarPFull + kRegions;         // [kRegions] P(i).V accumulated
-// One receive buffer holds one column half at a time: column half c of tile i
-// lands as phase i of RecvFull[c]; once the four softmax warps of that half
-// have read it, phase i of PeerFree[c] (in the sending CTA) completes.  Every
-// waiter waits for phase i of a barrier whose phase i - 1 is already complete,
-// so the parity test is unambiguous.
+// Each column half has its own receive slot: column half c of tile i lands
+// in slot c as phase i of RecvFull[c]; once the four softmax warps of that
+// half have read it, phase i of PeerFree[c] (in the sending CTA) completes, and
+// half c of tile i + 1 may be sent.  The two halves of a tile travel
+// independently.  Every waiter waits for phase i of a barrier whose phase
+// i - 1 is already complete, so the parity test is unambiguous.
 constexpr int kBarRecvFull = kBarPvDone + kRegions;      // [2]
 constexpr int kBarPeerFree = kBarRecvFull + 2;           // [2]
 constexpr int kBarPairA = kBarPeerFree + 2;              // [4]
@@ -476,11 +477,11 @@ __device__ void gather_role(const Params& p, const Ctx& c, int gw, int lane) {
 
 // ------------------------------------------------------------------ sender warps
 // Copy the CTA's partial score tile (128 heads x 64 keys, fp32) into the
-// peer's receive buffer, one column half at a time: TMEM -> registers -> the
+// peer's receive slots, one column half at a time: TMEM -> registers -> the
 // local staging buffer, then bulk copies by the TMA engine, so the CTA-to-CTA
 // traffic never queues in front of the softmax warps' shared-memory accesses.
-// Column half 0 of tile j may be copied once the peer has read half 1 of tile
-// j - 1 out of the buffer, half 1 once it has read half 0 of tile j.
+// Column half c of tile j goes to slot c once the peer has read half c of
+// tile j - 1 out of it.
 __device__ __forceinline__ bool send_half(const Ctx& c, const uint32_t (&v)[32], int h, int q, int lane, int j,
                                           int half, uint32_t stg, uint32_t dst, uint32_t rbar) {
   if (lane == 0) bulk_wait_read_all();  // the previous copy has left the staging buffer
@@ -491,8 +492,7 @@ __device__ __forceinline__ bool send_half(const Ctx& c, const uint32_t (&v)[32],
   __syncwarp();
   bool ok = true;
   if (lane == 0) {
-    if (half == 0 && j > 0) ok = mbar_wait<true>(c.bar(kBarPeerFree + 1), (j - 1) & 1, c.abort, kWaitLimitNs);
-    if (half == 1) ok = mbar_wait<true>(c.bar(kBarPeerFree + 0), j & 1, c.abort, kWaitLimitNs);
+    if (j > 0) ok = mbar_wait<true>(c.bar(kBarPeerFree + half), (j - 1) & 1, c.abort, kWaitLimitNs);
     if (ok) {
       const uint32_t blk = static_cast<uint32_t>(q) * kXchgBlockBytes;
       bulk_copy_to_peer(dst + blk, stg + blk, kXchgBlockBytes, rbar);
@@ -523,7 +523,7 @@ __device__ void sender_role(const Params& p, const Ctx& c, int q, int lane) {
     tc_fence_before();
     mbar_arrive_relaxed(c.bar(kBarSFree + r));  // the values are in registers (wait::ld)
     if (!send_half(c, a, h, q, lane, j, 0, stg, dst, rbar0)) break;
-    if (!send_half(c, b, h, q, lane, j, 1, stg, dst, rbar1)) break;
+    if (!send_half(c, b, h, q, lane, j, 1, stg, dst + kXchgBytes, rbar1)) break;
   }
   // the peer cannot leave before this CTA reaches its final cluster barrier,
   // which waits for these copies to complete
@@ -727,7 +727,7 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
         // into it only after that), so each phase is armed exactly once
         if (lane == 0 && q == 0 && j + 1 < c.total) mbar_arrive_expect_tx(c.bar(kBarRecvFull + half), kXchgBytes);
         float s[32];
-        const uint32_t slot = c.sbase + kOffRecv;
+        const uint32_t slot = c.sbase + kOffRecv + half * kXchgBytes;
         uint32_t dep = 0;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {

@@ -3,7 +3,11 @@ mla_cache.h and mla_prolog.h.
 
 Argument marshalling only: shapes and dtypes are read off torch tensors, the
 device pointers and the current CUDA stream are passed through, and a
-negative status becomes an exception.  Every step of the computation runs in
+negative status becomes an exception.  With the environment variable
+MLA_SPARSE_DEBUG set (to anything but "" or "0") every call also synchronises
+its stream and raises MlaError when the device status word of its operation
+has a bit set (a bad block id, a wait that ran out), instead of leaving it for
+a later *_device_status call.  Every step of the computation runs in
 the CUDA library; there is no other implementation to fall back to, and a
 missing library is an error.
 """
@@ -135,6 +139,21 @@ def _check(status: int):
         raise MlaError(status, load_library().mla_sparse_last_error().decode())
 
 
+def debug_enabled() -> bool:
+    """True when MLA_SPARSE_DEBUG asks for a status check after every call."""
+    return os.environ.get("MLA_SPARSE_DEBUG", "") not in ("", "0")
+
+
+def _debug_status(read_status, what: str, stream):
+    """Under MLA_SPARSE_DEBUG: synchronise, read and clear the operation's
+    status word, raise MlaError(MLA_ERR_DEVICE_STATUS) if a bit was set."""
+    if not debug_enabled():
+        return
+    flags = read_status(clear=True, stream=stream)
+    if flags:
+        raise MlaError(-7, f"{what}: device status {flags:#x} after the call (MLA_SPARSE_DEBUG)")
+
+
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
@@ -185,6 +204,7 @@ def mla_sparse_attn_fwd(q_nope, q_rope, kv_nope, kv_rope, kv_scales, topk_idx, b
                                  _ptr(act_seqs), _ptr(out), _ptr(lse), ctypes.c_float(softmax_scale),
                                  ctypes.c_int32(int(mode)), _stream_handle(stream))
     _check(st)
+    _debug_status(device_status, "mla_sparse_attn_fwd", stream)
     return out, lse
 
 
@@ -211,6 +231,7 @@ def mla_swa_fwd(q_nope, q_rope, kv_nope, kv_rope, kv_scales, block_table, act_se
                          ctypes.c_int32(int(window)), _ptr(out), _ptr(lse), ctypes.c_float(softmax_scale),
                          ctypes.c_int32(int(mode)), _stream_handle(stream))
     _check(st)
+    _debug_status(device_status, "mla_swa_fwd", stream)
     return out, lse
 
 
@@ -243,6 +264,7 @@ def mla_compressed_attn_fwd(q_nope, q_rope, kv_nope, kv_rope, kv_scales, block_t
                                      ctypes.c_float(softmax_scale), ctypes.c_int32(int(mode)),
                                      _stream_handle(stream))
     _check(st)
+    _debug_status(device_status, "mla_compressed_attn_fwd", stream)
     return out, lse
 
 
@@ -288,6 +310,7 @@ def mla_indexer_topk(q, w, k_cache, block_table, act_seqs, topk_idx, workspace, 
     st = lib.mla_indexer_topk(ctypes.byref(dims), _ptr(q), _ptr(w), _ptr(k_cache), _ptr(block_table), _ptr(act_seqs),
                               _ptr(topk_idx), _ptr(workspace), ctypes.c_size_t(nbytes), _stream_handle(stream))
     _check_idx(st)
+    _debug_status(indexer_device_status, "mla_indexer_topk", stream)
     return topk_idx
 
 
@@ -299,6 +322,7 @@ def mla_indexer_scores(q, w, k_cache, block_table, act_seqs, scores, *, dims: In
     st = lib.mla_indexer_scores(ctypes.byref(dims), _ptr(q), _ptr(w), _ptr(k_cache), _ptr(block_table),
                                 _ptr(act_seqs), _ptr(scores), ctypes.c_size_t(nbytes), _stream_handle(stream))
     _check_idx(st)
+    _debug_status(indexer_device_status, "mla_indexer_scores", stream)
     return scores
 
 
@@ -309,6 +333,7 @@ def mla_indexer_select(scores, act_seqs, topk_idx, *, dims: IndexerDims, stream=
     st = lib.mla_indexer_select(ctypes.byref(dims), _ptr(scores), _ptr(act_seqs), _ptr(topk_idx),
                                 _stream_handle(stream))
     _check_idx(st)
+    _debug_status(indexer_device_status, "mla_indexer_select", stream)
     return topk_idx
 
 
@@ -321,6 +346,7 @@ def mla_indexer_topk_noalloc(q, w, k_cache, block_table, act_seqs, topk_idx, *, 
     st = lib.mla_indexer_topk_noalloc(ctypes.byref(dims), _ptr(q), _ptr(w), _ptr(k_cache), _ptr(block_table),
                                       _ptr(act_seqs), _ptr(topk_idx), _stream_handle(stream))
     _check_idx(st)
+    _debug_status(indexer_device_status, "mla_indexer_topk_noalloc", stream)
     return topk_idx
 
 
@@ -346,6 +372,7 @@ def mla_cache_write(k_nope, k_rope, cache_index, kv_nope, kv_rope, kv_scales=Non
                              _stream_handle(stream))
     if st != MLA_OK:
         raise MlaError(st, lib.mla_cache_last_error().decode())
+    _debug_status(cache_device_status, "mla_cache_write", stream)
 
 
 def cache_device_status(clear: bool = True, stream=None) -> int:
@@ -397,6 +424,7 @@ def mla_prolog(x, wq_a, gamma_cq, wq_b, w_uk, wkv, gamma_ckv, cos, sin, cache_in
                         _stream_handle(stream))
     if st != MLA_OK:
         raise MlaError(st, lib.mla_prolog_last_error().decode())
+    _debug_status(prolog_device_status, "mla_prolog", stream)
     return q_nope, q_rope
 
 

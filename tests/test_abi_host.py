@@ -334,3 +334,13 @@ def test_prolog_argument_errors_are_reported_before_launch(lib, case, expect):
     assert st == expect, (case, st, lib.mla_prolog_last_error())
     if expect != 0:
         assert lib.mla_prolog_last_error()
+
+
+def test_debug_switch_reads_the_environment(monkeypatch):
+    from mla_sparse_top_gb300 import binding
+    monkeypatch.delenv("MLA_SPARSE_DEBUG", raising=False)
+    assert not binding.debug_enabled()
+    monkeypatch.setenv("MLA_SPARSE_DEBUG", "0")
+    assert not binding.debug_enabled()
+    monkeypatch.setenv("MLA_SPARSE_DEBUG", "1")
+    assert binding.debug_enabled()

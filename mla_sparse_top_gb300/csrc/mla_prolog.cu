@@ -393,29 +393,6 @@ mla_status mla_prolog(const mla_prolog_dims* dims, const void* x, const mla_prol
   np.int8 = dims->kv_int8;
   np.eps = dims->eps;
 
-  // key path on the side stream, forked from `s` here and joined back at the end
-  PRO_CUDA(cudaEventRecord(st.fork, s), "recording the fork event");
-  PRO_CUDA(cudaStreamWaitEvent(st.side, st.fork, 0), "side stream wait");
-  PRO_BLAS(cublasSetStream(st.blas, st.side), "cublasSetStream");
-  PRO_BLAS(cublasSetWorkspace(st.blas, ws + L.ws_side, kBlasWsSide), "cublasSetWorkspace");
-  mla_status gs = gemm_rm(st.blas, T, kKv, hidden, x, hidden, w->wkv, kKv, kv_raw, kKv, CUDA_R_32F, "x @ wkv");
-  if (gs != MLA_OK) return gs;
-  kv_rows_kernel<<<static_cast<unsigned>((T + kWarps - 1) / kWarps), kWarps * 32, 0, st.side>>>(np);
-  PRO_CUDA(cudaGetLastError(), "kv_rows_kernel launch");
-  PRO_CUDA(cudaEventRecord(st.join, st.side), "recording the join event");
-
-  // query path on `s`
-  PRO_BLAS(cublasSetStream(st.blas, s), "cublasSetStream");
-  PRO_BLAS(cublasSetWorkspace(st.blas, ws + L.ws_main, kBlasWsMain), "cublasSetWorkspace");
-  gs = gemm_rm(st.blas, T, q_lora, hidden, x, hidden, w->wq_a, q_lora, c_raw, q_lora, CUDA_R_32F, "x @ wq_a");
-  if (gs != MLA_OK) return gs;
-  cq_rows_kernel<<<static_cast<unsigned>(T), kCqThreads, 0, s>>>(np);
-  PRO_CUDA(cudaGetLastError(), "cq_rows_kernel launch");
-
-  gs = gemm_rm(st.blas, T, H * kQHead, q_lora, c_q, q_lora, w->wq_b, H * kQHead, q_raw, H * kQHead, CUDA_R_32F,
-               "c^Q @ wq_b");
-  if (gs != MLA_OK) return gs;
-
   HeadParams hp;
   hp.q_raw = q_raw;
   hp.cos = cos;
@@ -425,17 +402,46 @@ mla_status mla_prolog(const mla_prolog_dims* dims, const void* x, const mla_prol
   hp.H = H;
   hp.TH = T * H;
   hp.eps = dims->eps;
-  q_heads_kernel<<<static_cast<unsigned>((static_cast<int64_t>(T) * H + kWarps - 1) / kWarps), kWarps * 32, 0, s>>>(hp);
-  PRO_CUDA(cudaGetLastError(), "q_heads_kernel launch");
 
-  // absorption: head h, C_h[T, 512] (row stride H * 512) = q_n[:, h] [T, 128] (row stride H * 128) @ w_uk[h]
-  const float one = 1.f, zero = 0.f;
-  PRO_BLAS(cublasGemmStridedBatchedEx(st.blas, CUBLAS_OP_N, CUBLAS_OP_N, kLatent, T, kQkNope, &one, w->w_uk,
-                                      CUDA_R_16BF, kLatent, static_cast<long long>(kQkNope) * kLatent, q_n,
-                                      CUDA_R_16BF, H * kQkNope, kQkNope, &zero, q_nope, CUDA_R_16BF, H * kLatent,
-                                      kLatent, H, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT),
-           "absorption q_nope @ w_uk");
-  PRO_CUDA(cudaStreamWaitEvent(s, st.join, 0), "join wait");
+  // key path on the side stream, forked from `s` here; whatever the paths enqueue, the side stream is
+  // joined back into `s` before returning, also when a step fails part-way
+  PRO_CUDA(cudaEventRecord(st.fork, s), "recording the fork event");
+  PRO_CUDA(cudaStreamWaitEvent(st.side, st.fork, 0), "side stream wait");
+  auto paths = [&]() -> mla_status {
+    PRO_BLAS(cublasSetStream(st.blas, st.side), "cublasSetStream");
+    PRO_BLAS(cublasSetWorkspace(st.blas, ws + L.ws_side, kBlasWsSide), "cublasSetWorkspace");
+    mla_status gs = gemm_rm(st.blas, T, kKv, hidden, x, hidden, w->wkv, kKv, kv_raw, kKv, CUDA_R_32F, "x @ wkv");
+    if (gs != MLA_OK) return gs;
+    kv_rows_kernel<<<static_cast<unsigned>((T + kWarps - 1) / kWarps), kWarps * 32, 0, st.side>>>(np);
+    PRO_CUDA(cudaGetLastError(), "kv_rows_kernel launch");
+
+    // query path on `s`
+    PRO_BLAS(cublasSetStream(st.blas, s), "cublasSetStream");
+    PRO_BLAS(cublasSetWorkspace(st.blas, ws + L.ws_main, kBlasWsMain), "cublasSetWorkspace");
+    gs = gemm_rm(st.blas, T, q_lora, hidden, x, hidden, w->wq_a, q_lora, c_raw, q_lora, CUDA_R_32F, "x @ wq_a");
+    if (gs != MLA_OK) return gs;
+    cq_rows_kernel<<<static_cast<unsigned>(T), kCqThreads, 0, s>>>(np);
+    PRO_CUDA(cudaGetLastError(), "cq_rows_kernel launch");
+    gs = gemm_rm(st.blas, T, H * kQHead, q_lora, c_q, q_lora, w->wq_b, H * kQHead, q_raw, H * kQHead, CUDA_R_32F,
+                 "c^Q @ wq_b");
+    if (gs != MLA_OK) return gs;
+    q_heads_kernel<<<static_cast<unsigned>((static_cast<int64_t>(T) * H + kWarps - 1) / kWarps), kWarps * 32, 0,
+                     s>>>(hp);
+    PRO_CUDA(cudaGetLastError(), "q_heads_kernel launch");
+    // absorption: head h, C_h[T, 512] (row stride H * 512) = q_n[:, h] [T, 128] (row stride H * 128) @ w_uk[h]
+    const float one = 1.f, zero = 0.f;
+    PRO_BLAS(cublasGemmStridedBatchedEx(st.blas, CUBLAS_OP_N, CUBLAS_OP_N, kLatent, T, kQkNope, &one, w->w_uk,
+                                        CUDA_R_16BF, kLatent, static_cast<long long>(kQkNope) * kLatent, q_n,
+                                        CUDA_R_16BF, H * kQkNope, kQkNope, &zero, q_nope, CUDA_R_16BF, H * kLatent,
+                                        kLatent, H, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT),
+             "absorption q_nope @ w_uk");
+    return MLA_OK;
+  };
+  const mla_status body = paths();
+  cudaError_t ej = cudaEventRecord(st.join, st.side);
+  if (ej == cudaSuccess) ej = cudaStreamWaitEvent(s, st.join, 0);
+  if (body != MLA_OK) return body;  // its message stands
+  if (ej != cudaSuccess) return pro_fail(MLA_ERR_CUDA, "joining the side stream: %s", cudaGetErrorString(ej));
   return MLA_OK;
 }
 

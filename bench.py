@@ -479,6 +479,16 @@ def main():
         dist.barrier()
     times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     status = mla.device_status(clear=True)
+    # warm: the same call back to back with no flush in between (L2 keeps what fits)
+    n_warm = 20
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launch()
+    w0.record(stream)
+    for _ in range(n_warm):
+        launch()
+    w1.record(stream)
+    torch.cuda.synchronize()
+    warm_us = w0.elapsed_time(w1) * 1000.0 / n_warm
 
     # end-to-end through the C ABI with host buffers (pinned), copies inside the timed region
     per_call = ["q_nope", "q_rope", "block_table", "act_seqs"]
@@ -510,9 +520,11 @@ def main():
     e2e_ms = [s.elapsed_time(e) for s, e in zip(e_s, e_e)]
     clock_summary = clocks.stop()
 
-    us = float(np.mean(times_ms) * 1000.0)
-    e2e_us = float(np.mean(e2e_ms) * 1000.0)
-    us, e2e_us = reduce_max_over_ranks([us, e2e_us], device="cuda")
+    # median of the cold-L2 calls (the headline); mean and the warm back-to-back figure beside it
+    us = float(np.median(times_ms) * 1000.0)
+    mean_us = float(np.mean(times_ms) * 1000.0)
+    e2e_us = float(np.median(e2e_ms) * 1000.0)
+    us, e2e_us, mean_us, warm_us = reduce_max_over_ranks([us, e2e_us, mean_us, warm_us], device="cuda")
 
     if rank == 0:
         hbm_gbs, bf16_tf, peak_src = measured_peaks()
@@ -534,6 +546,8 @@ def main():
             "dtype": "bf16",
             "data": "synthetic",
             "config": run_config(args.workload, d, world, inp.get("window")),
+            "timing": {"statistic": "median of cold-L2 calls", "mean_us": round(mean_us, 3),
+                       "warm_back_to_back_us": round(warm_us, 3), "l2_flush": "256 MiB write between calls"},
             "gathered_kv_tbps": round(counts["gathered_bytes"] * world / (us * 1e-6) / 1e12, 4),
             "tflops": round(tflops * world, 2),
             "roofline_us": round(roofline_us, 3),
@@ -1176,17 +1190,21 @@ def run_reference(args, world, rank):
     toks_per_step = max(1, cores)
     if args.warmup > 0:
         oracle_call(inp, tokens=[0])
-    per_call = []
+    per_call, step_s = [], []
     for i in range(args.steps):
         toks = [(i * toks_per_step + k) % T for k in range(toks_per_step)]
         t0 = time.perf_counter()
         oracle_call(inp, tokens=toks)
-        per_call.append((time.perf_counter() - t0) / len(toks) * T * 1e6)
+        step_s.append(time.perf_counter() - t0)
+        per_call.append(step_s[-1] / len(toks) * T * 1e6)
     us = float(np.mean(per_call))
     sample = f"{toks_per_step} of {T} tokens per step, scaled to all {T} tokens"
     line = {
         "metric": metric_of(inp), "value": round(us, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(us / 1000.0, 3), "higher_is_better": False, "scaling": "weak",
+        # a step is the token sample; value is the whole call extrapolated from it
+        "warmup": args.warmup, "ms_per_step": round(float(np.mean(step_s)) * 1000.0, 3),
+        "value_kind": "per-call time extrapolated from the sampled tokens of each step",
+        "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
         "config": run_config(args.workload, d, world, inp.get("window")),
         "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},

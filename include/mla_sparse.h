@@ -21,7 +21,8 @@
  *
  * Conventions
  *   - Every data pointer is a DEVICE pointer owned by the caller; the library
- *     allocates nothing and keeps no state besides a sticky device status word.
+ *     allocates nothing and keeps no state besides a device status word and
+ *     the bound of its device-side waits.
  *   - All tensors are dense row-major with the shapes given below.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream) and never synchronise.
@@ -31,11 +32,14 @@
  *   - Bad block ids for valid indices (outside [0, num_blocks), or a table
  *     slot index / 128 beyond max_blocks_per_seq) never fault: the entry is
  *     masked out of the softmax and MLA_DEVICE_BAD_BLOCK is raised in the
- *     device status word.  Every internal wait of the kernel is bounded; a
- *     wait that runs out raises MLA_DEVICE_TIMEOUT (sticky: later launches do
- *     no work until the status is cleared).
+ *     device status word.  Every internal wait of the kernel is bounded (500 ms
+ *     unless mla_sparse_set_wait_limit_ns says otherwise); a wait that runs
+ *     out makes that launch give up (its out/lse are then unspecified) and
+ *     raises MLA_DEVICE_TIMEOUT.  Status bits accumulate until cleared; a
+ *     later launch still runs in full.
  *   - Numerics: inputs bf16; products are exact; score and output
- *     accumulation in fp32 on the tensor cores; the softmax weights P enter
+ *     accumulation in fp32 on the tensor cores (the two CTAs of a cluster
+ *     work as one pair: each owns 64 of the 128 heads); the softmax weights P enter
  *     the P.V product as two bf16 terms, P_hi = bf16(p) and
  *     P_lo = bf16(p - P_hi), so their relative error stays below 2^-18; the
  *     values are the bf16 cache rows themselves; out is rounded to bf16 once.
@@ -181,6 +185,25 @@ const char* mla_sparse_last_error(void);
  * MLA_ERR_CUDA on a runtime error, MLA_OK otherwise.
  */
 mla_status mla_sparse_device_status(void* stream, uint32_t* flags, int32_t clear);
+
+/*
+ * mla_sparse_get_device_status -- the status query under the name of the
+ * boundary's original list: mla_sparse_device_status(stream, NULL, 0), i.e.
+ * synchronise, report without clearing.
+ */
+mla_status mla_sparse_get_device_status(void* stream);
+
+/*
+ * mla_sparse_set_wait_limit_ns -- bound, in nanoseconds, of every device-side
+ * wait of the attention launches enqueued after this call (all threads of the
+ * process; default 500 ms).  No counterpart in the pages: the pages' runtime
+ * debug mode ("DeepSeek V3/V2 Sparse Flash Attention with Quantization",
+ * notes) checks the operator while it runs; this bound is what turns a stall
+ * into MLA_DEVICE_TIMEOUT instead of a hang.  Accepted range [1 us, 60 s];
+ * MLA_ERR_SHAPE otherwise.  A short bound makes a launch whose waits take
+ * longer give up, which the tests use to exercise the timeout path.
+ */
+mla_status mla_sparse_set_wait_limit_ns(uint64_t ns);
 
 /* ABI version of this header (major * 100 + minor). */
 int32_t mla_sparse_abi_version(void);

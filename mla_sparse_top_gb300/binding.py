@@ -30,6 +30,7 @@ MLA_DEVICE_BAD_BLOCK = 0x1
 MLA_DEVICE_TIMEOUT = 0x2
 
 EXPORTED_SYMBOLS = ("mla_sparse_attn_fwd", "mla_swa_fwd", "mla_compressed_attn_fwd", "mla_sparse_last_error", "mla_sparse_device_status",
+                    "mla_sparse_get_device_status", "mla_sparse_set_wait_limit_ns",
                     "mla_sparse_abi_version", "mla_indexer_workspace_bytes", "mla_indexer_topk",
                     "mla_indexer_scores", "mla_indexer_select", "mla_indexer_device_status",
                     "mla_indexer_last_error", "mla_indexer_topk_noalloc", "mla_cache_write",
@@ -99,6 +100,10 @@ def load_library(path: str = LIB_PATH):
     lib.mla_sparse_last_error.restype = ctypes.c_char_p
     lib.mla_sparse_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int32]
     lib.mla_sparse_device_status.restype = ctypes.c_int
+    lib.mla_sparse_get_device_status.argtypes = [vp]
+    lib.mla_sparse_get_device_status.restype = ctypes.c_int
+    lib.mla_sparse_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.mla_sparse_set_wait_limit_ns.restype = ctypes.c_int
     lib.mla_sparse_abi_version.argtypes = []
     lib.mla_sparse_abi_version.restype = ctypes.c_int32
     lib.mla_indexer_workspace_bytes.argtypes = [ctypes.POINTER(IndexerDims)]
@@ -280,6 +285,14 @@ def device_status(clear: bool = True, stream=None) -> int:
 
 def abi_version() -> int:
     return int(load_library().mla_sparse_abi_version())
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    """Bound of every device-side wait of later attention launches."""
+    _check(load_library().mla_sparse_set_wait_limit_ns(int(ns)))
+
+
+DEFAULT_WAIT_LIMIT_NS = 500 * 1000 * 1000
 
 
 # ------------------------------------------------------------------ Lightning Indexer

@@ -53,6 +53,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "../../include/mla_sparse.h"
@@ -147,8 +148,6 @@ constexpr uint32_t kTmemRegion = 256;  // + 64 * (i % kRegions)
 constexpr uint32_t kTmemQ = 448;
 static_assert(kTmemRegion + 64 * kRegions <= kTmemQ && kTmemQ + 64 == kTmemCols, "TMEM layout");
 
-constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;
-
 __device__ unsigned int g_mla_status = 0;
 
 struct Params {
@@ -174,6 +173,7 @@ struct Params {
   const int32_t* cmp_idx;  // SCFA lists [T, cmp_topk]; nullptr: CFA (every visible entry)
   int cmp_num_blocks, cmp_mbps, cmp_ratio, cmp_topk;
   float scale_log2;
+  unsigned long long wait_ns;  // bound of every wait
 };
 
 struct Ctx {
@@ -184,6 +184,7 @@ struct Ctx {
   int cid;    // cluster index
   int ntok;   // tokens of this cluster
   int total;  // key tiles of this cluster: ntok * n_tiles, one stream across its tokens
+  uint64_t wait_ns;
   volatile uint32_t* abort;
   __device__ uint32_t bar(int i) const { return sbase + kOffBars + 8 * i; }
 };
@@ -192,7 +193,7 @@ struct Ctx {
 __device__ __forceinline__ int token_of(const Params& p, const Ctx& c, int m) { return c.cid + m * p.n_clusters; }
 
 __device__ __forceinline__ bool wait_bar(const Ctx& c, int idx, uint32_t parity) {
-  return mbar_wait<false>(c.bar(idx), parity, c.abort, kWaitLimitNs);
+  return mbar_wait<false>(c.bar(idx), parity, c.abort, c.wait_ns);
 }
 // Warp-uniform waits: every lane waits (bounded) and the warp agrees on the
 // outcome, so warp-collective instructions after it never see a partial warp.
@@ -200,7 +201,7 @@ __device__ __forceinline__ bool warp_wait(const Ctx& c, int idx, uint32_t parity
   return __all_sync(0xffffffffu, wait_bar(c, idx, parity));
 }
 __device__ __forceinline__ bool warp_wait_cluster(const Ctx& c, int idx, uint32_t parity) {
-  return __all_sync(0xffffffffu, mbar_wait<true>(c.bar(idx), parity, c.abort, kWaitLimitNs));
+  return __all_sync(0xffffffffu, mbar_wait<true>(c.bar(idx), parity, c.abort, c.wait_ns));
 }
 
 __device__ __forceinline__ uint4 ldg16(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
@@ -473,6 +474,7 @@ __device__ void gather_role(const Params& p, const Ctx& c, int gw, int lane) {
       mbar_arrive(c.bar(kBarFull + st));
     }
   }
+  cp_async_wait_all();  // no copy of this thread lands after the CTA has left its roles
 }
 
 // ------------------------------------------------------------------ sender warps
@@ -492,7 +494,7 @@ __device__ __forceinline__ bool send_half(const Ctx& c, const uint32_t (&v)[32],
   __syncwarp();
   bool ok = true;
   if (lane == 0) {
-    if (j > 0) ok = mbar_wait<true>(c.bar(kBarPeerFree + half), (j - 1) & 1, c.abort, kWaitLimitNs);
+    if (j > 0) ok = mbar_wait<true>(c.bar(kBarPeerFree + half), (j - 1) & 1, c.abort, c.wait_ns);
     if (ok) {
       const uint32_t blk = static_cast<uint32_t>(q) * kXchgBlockBytes;
       bulk_copy_to_peer(dst + blk, stg + blk, kXchgBlockBytes, rbar);
@@ -623,12 +625,12 @@ __device__ void mma_role(const Params& p, const Ctx& c) {
       const uint64_t now = globaltimer_ns();
       if (t_idle == 0 || spins == 256u) t_idle = now;
       if (*c.abort) ok = false;
-      else if (now - t_idle > kWaitLimitNs) { *c.abort = 1u; ok = false; }
+      else if (now - t_idle > c.wait_ns) { *c.abort = 1u; ok = false; }
     }
   }
   umma_commit(c.bar(kBarFinal));
   volatile uint32_t never = 0;
-  mbar_wait<false>(c.bar(kBarFinal), 0, &never, kWaitLimitNs);
+  mbar_wait<false>(c.bar(kBarFinal), 0, &never, c.wait_ns > 500000000ull ? c.wait_ns : 500000000ull);
 }
 
 // ------------------------------------------------------------------ softmax warps
@@ -875,10 +877,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_spa
   c.ntok = (p.T - c.cid + p.n_clusters - 1) / p.n_clusters;
   c.total = c.ntok * p.n_tiles;
   c.abort = reinterpret_cast<volatile uint32_t*>(smem + kOffAbort);
+  c.wait_ns = p.wait_ns;
   if (tid == 0) {
     // the swizzled operand layouts need a 1024-byte aligned base
     const bool misaligned = (c.sbase & 1023u) != 0;
-    *c.abort = ((*reinterpret_cast<volatile unsigned int*>(&g_mla_status) & MLA_DEVICE_TIMEOUT) || misaligned) ? 1u : 0u;
+    *c.abort = misaligned ? 1u : 0u;
     if (misaligned) atomicOr(&g_mla_status, MLA_DEVICE_TIMEOUT);
     for (int i = 0; i < kStages; ++i) {
       mbar_init(c.bar(kBarFull + i), kInt8 ? 256 : 256 + 8);
@@ -976,6 +979,9 @@ cudaError_t g_attr_err[kMaxDevices][6];
 
 int g_max_clusters[kMaxDevices][6];
 
+// Bound of every device-side wait of the next launches (nanoseconds).
+std::atomic<unsigned long long> g_wait_ns{500ull * 1000ull * 1000ull};
+
 // Also records how many two-CTA clusters of the kernel the device runs at once.
 template <bool kInt8, int kMode>
 cudaError_t prepare_kernel(int dev) {
@@ -1019,7 +1025,7 @@ cudaError_t prepare_kernel(int dev) {
 
 extern "C" {
 
-int32_t mla_sparse_abi_version(void) { return 100; }
+int32_t mla_sparse_abi_version(void) { return 200; }
 
 const char* mla_sparse_last_error(void) { return g_last_error; }
 
@@ -1118,6 +1124,7 @@ mla_status attn_fwd(const mla_dims* dims, const void* q_nope, const void* q_rope
   p.mbps = d.max_blocks_per_seq;
   p.n_tiles = (d.topk + mlasp::kTileKeys - 1) / mlasp::kTileKeys;
   p.scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634);
+  p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
   // persistent clusters: as many as run at once (never more than tokens); cluster
   // c takes tokens c, c + n_clusters, ... as one stream of key tiles
   const int max_clusters = g_max_clusters[dev][kv];
@@ -1184,6 +1191,16 @@ mla_status mla_compressed_attn_fwd(const mla_dims* dims, const void* q_nope, con
   return attn_fwd(dims, q_nope, q_rope, kv_nope, kv_rope, kv_scales, nullptr, window, cmp, block_table, act_seqs, out,
                   lse, softmax_scale, mode, stream);
 }
+
+mla_status mla_sparse_set_wait_limit_ns(uint64_t ns) {
+  g_last_error[0] = '\0';
+  if (ns < 1000ull || ns > 60ull * 1000ull * 1000ull * 1000ull)
+    return fail(MLA_ERR_SHAPE, "wait limit %llu ns outside [1 us, 60 s]", static_cast<unsigned long long>(ns));
+  g_wait_ns.store(ns, std::memory_order_relaxed);
+  return MLA_OK;
+}
+
+mla_status mla_sparse_get_device_status(void* stream) { return mla_sparse_device_status(stream, nullptr, 0); }
 
 mla_status mla_sparse_device_status(void* stream, uint32_t* flags, int32_t clear) {
   g_last_error[0] = '\0';

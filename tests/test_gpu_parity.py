@@ -38,10 +38,13 @@ def check_full(inp, label, mode=None):
     return out, lse
 
 
-def check_sampled(inp, label, n_sample=8, seed=0):
+def check_sampled(inp, label, n_sample=8, seed=0, tokens=None):
     T = inp["dims"]["B"] * inp["dims"]["S1"]
-    rng = np.random.default_rng(seed)
-    toks = sorted(set([0, T - 1] + rng.choice(T, size=min(T, n_sample), replace=False).tolist()))
+    if tokens is None:
+        rng = np.random.default_rng(seed)
+        toks = sorted(set([0, T - 1] + rng.choice(T, size=min(T, n_sample), replace=False).tolist()))
+    else:
+        toks = sorted(set(int(t) for t in tokens))
     out, lse, status = run_gpu(inp)
     ref_out, ref_lse, bad = oracle.forward(inp, tokens=toks)
     assert status & 2 == 0, f"{label}: device timeout"
@@ -164,7 +167,9 @@ def test_large_logits_trigger_rescale():
 
 
 def test_softmax_scale_variants():
-    for scale in (0.01, 0.3):
+    """Positive scales take the row max on raw scores; zero and negative
+    scales scale every score before the max (the other branch)."""
+    for scale in (0.01, 0.3, 0.0, -0.05, -1.0):
         inp = workloads.make_inputs(B=1, S1=2, n_q=128, act_seqs=[900], topk=256, seed=33, softmax_scale=scale)
         check_full(inp, f"scale={scale}")
 
@@ -182,11 +187,24 @@ def test_deterministic_and_permutation_stable():
     assert_out_close(c[0], ref_out, "permuted list")
 
 
-# ------------------------------------------------------------ full-size workloads, sampled tokens
-@pytest.mark.parametrize("name", ["mtp_decode", "int8_decode", "varlen_decode", "prefill"])
-def test_full_size_workload_sampled(name):
+# ------------------------------------------------------------ full-size workloads
+# The launch configuration the benchmark times.  The 128-token decode
+# workloads are checked on every token; the 4096-token prefill on 274 tokens,
+# every 15th one plus the last (15 is prime to the number of clusters, so the
+# sample covers every cluster and many stream positions).
+@pytest.mark.parametrize("name", ["mtp_decode", "int8_decode", "varlen_decode"])
+def test_full_size_decode_every_token(name):
     inp = workloads.NAMED[name]()
-    check_sampled(inp, name, n_sample=6)
+    T = inp["dims"]["B"] * inp["dims"]["S1"]
+    check_sampled(inp, name, tokens=range(T))
+
+
+def test_full_size_prefill_strided_tokens():
+    inp = workloads.NAMED["prefill"]()
+    T = inp["dims"]["B"] * inp["dims"]["S1"]
+    toks = list(range(0, T, 15)) + [T - 1]
+    assert len(set(toks)) >= 256 and 0 in toks and T - 1 in toks
+    check_sampled(inp, "prefill", tokens=toks)
 
 
 # ------------------------------------------------------------ persistent clusters: token streams

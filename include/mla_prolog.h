@@ -31,15 +31,14 @@
  *
  * Conventions are those of mla_sparse.h: device pointers owned by the caller,
  * asynchronous on `stream`, argument errors returned before any launch with
- * mla_prolog_last_error() describing them.  The products are cuBLAS GEMMs; the
- * norms, rotations and the cache write are this library's kernels.  The key
- * path (its projection, norm, rotation and cache write) runs on an internal
- * second stream that forks from `stream` and joins back into it through
- * events before the call's work on `stream` ends, so the call is capturable
- * into a CUDA graph.
- * The first call on each device creates that stream, the events and a cuBLAS
- * handle: make it before any stream capture begins.  Calls are serialised by
- * a lock (one handle per device).
+ * mla_prolog_last_error() describing them.  Every step runs in this
+ * library's kernels: the four matrix products in its tcgen05 product kernel
+ * (the weights streamed by TMA as the MMA's A operand, x @ wq_a and x @ wkv
+ * in one launch), the norms, rotations and the cache write in its row
+ * kernels; all six launches go to `stream`, so the call is capturable into a
+ * CUDA graph.  The first call on each device sets the product kernel's
+ * shared-memory attribute and looks up the driver's tensor-map encoder: make
+ * it before any stream capture begins.
  */
 #ifndef MLA_PROLOG_H_
 #define MLA_PROLOG_H_
@@ -73,8 +72,9 @@ typedef struct mla_prolog_weights {
   const void* gamma_ckv; /* bf16 [576] */
 } mla_prolog_weights;
 
-/* Bytes of workspace mla_prolog needs (fp32 projections, bf16 operands and
- * two cuBLAS workspaces); 0 for invalid dims. */
+/* Bytes of workspace mla_prolog needs (the fp32 partial sums of the
+ * projections over their k splits and the bf16 operands between the
+ * products); 0 for invalid dims. */
 size_t mla_prolog_workspace_bytes(const mla_prolog_dims* dims);
 
 /*

@@ -27,9 +27,9 @@ def cuda_home() -> str:
 
 
 def link_flags() -> list:
-    """cuBLAS (the MLA Prolog's plain GEMMs), found at run time through the toolkit's library directory."""
+    """The CUDA runtime and driver API (tensor-map encoding), found through the toolkit's library directory."""
     lib = os.path.join(cuda_home(), "lib64")
-    return ["-L" + lib, "-Xlinker", "-rpath=" + lib, "-lcublas"]
+    return ["-L" + lib, "-Xlinker", "-rpath=" + lib]
 
 
 def build(force: bool = False, verbose: bool = False) -> str:

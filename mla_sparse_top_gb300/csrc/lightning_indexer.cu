@@ -111,13 +111,6 @@ __device__ __forceinline__ bool warp_wait(const Ctx& c, int idx, uint32_t parity
   return __all_sync(0xffffffffu, wait_bar(c, idx, parity));
 }
 
-// 2-D TMA tiled load (box of the tensor map at coordinates {x, y}) into
-// shared memory, counted on `bar`.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y, uint32_t bar) {
-  asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-               :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar) : "memory");
-}
-
 // sum_h w[h] * ReLU(D[lane, col + h]) over H heads for this thread's key (TMEM
 // lane), NC x 16 heads per TMEM wait (H a multiple of 16 * NC), four partial
 // sums.  When `release` is set, the accumulator barrier is arrived on as soon

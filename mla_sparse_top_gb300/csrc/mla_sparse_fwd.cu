@@ -95,8 +95,8 @@ constexpr int kQHalfBytes = kHeads * 128 * 2;          // Q latent dims [128, 25
 constexpr int kQRopeBytes = kHeads * 64;
 
 constexpr int kOffRecv = 0;                            // [2] one slot per column half, same offset in both CTAs
-constexpr int kOffStaging = kOffRecv + 2 * kXchgBytes;
-constexpr int kOffStages = kOffStaging + kXchgBytes;
+constexpr int kOffStaging = kOffRecv + 2 * kXchgBytes;  // [2] one staging buffer per column half
+constexpr int kOffStages = kOffStaging + 2 * kXchgBytes;
 constexpr int kOffQHalf = kOffStages + kStages * kStageBytes;
 constexpr int kOffQRope = kOffQHalf + kQHalfBytes;
 constexpr int kOffRows = kOffQRope + kQRopeBytes;       // int32 [kIdxSlots][64]
@@ -486,7 +486,9 @@ __device__ void gather_role(const Params& p, const Ctx& c, int gw, int lane) {
 // tile j - 1 out of it.
 __device__ __forceinline__ bool send_half(const Ctx& c, const uint32_t (&v)[32], int h, int q, int lane, int j,
                                           int half, uint32_t stg, uint32_t dst, uint32_t rbar) {
-  if (lane == 0) bulk_wait_read_all();  // the previous copy has left the staging buffer
+  // this half's previous copy has left its staging buffer (the other half's
+  // most recent copy may still be reading its own)
+  if (lane == 0) bulk_wait_read_but_one();
   __syncwarp();
 #pragma unroll
   for (int k = 0; k < 8; ++k) sts16(stg + xchg_offset(h, k), make_uint4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]));
@@ -525,7 +527,7 @@ __device__ void sender_role(const Params& p, const Ctx& c, int q, int lane) {
     tc_fence_before();
     mbar_arrive_relaxed(c.bar(kBarSFree + r));  // the values are in registers (wait::ld)
     if (!send_half(c, a, h, q, lane, j, 0, stg, dst, rbar0)) break;
-    if (!send_half(c, b, h, q, lane, j, 1, stg, dst + kXchgBytes, rbar1)) break;
+    if (!send_half(c, b, h, q, lane, j, 1, stg + kXchgBytes, dst + kXchgBytes, rbar1)) break;
   }
   // the peer cannot leave before this CTA reaches its final cluster barrier,
   // which waits for these copies to complete

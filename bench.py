@@ -201,7 +201,8 @@ def ncu_traffic(workload, kernel=KERNEL_NAME, source=KERNEL_SOURCE):
 
 SEEDS = {"tiny_decode": 0, "mtp_decode": 1, "int8_decode": 2, "varlen_decode": 3, "prefill": 4, "swa_decode": 10,
          "indexer_decode": 5, "indexer_tiny": 6, "indexer_varlen": 7, "cache_write_decode": 8,
-         "cache_write_prefill": 9, "cfa_decode": 11, "scfa_decode": 12, "prolog_decode": 14, "prolog_prefill": 15}
+         "cache_write_prefill": 9, "cfa_decode": 11, "scfa_decode": 12, "prolog_decode": 14, "prolog_prefill": 15,
+         "mtp_decode_b2": 16}
 
 
 def rank_seed(workload: str, rank: int) -> int:
@@ -467,12 +468,14 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     clocks.mark_on()
+    launches0 = mla.launch_count()
     for i in range(args.steps):
         flush.fill_(float(i))
         spin_gpu()
         starts[i].record(stream)
         launch()
         ends[i].record(stream)
+    launches = mla.launch_count() - launches0
     torch.cuda.synchronize()
     clocks.mark_off()
     if world > 1:
@@ -557,7 +560,7 @@ def main():
                        "frac": round(tflops / bf16_tf, 4), "flops_per_launch": counts["flops"]},
             "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h)},
-            "gpu_launches": args.steps,
+            "gpu_launches": launches,
             "clocks": clock_summary,
             "device_status": status,
         }

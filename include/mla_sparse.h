@@ -20,9 +20,18 @@
  *   out = 0 and lse = -inf.  Repeated indices count once per occurrence.
  *
  * Conventions
- *   - Every data pointer is a DEVICE pointer owned by the caller; the library
- *     allocates nothing and keeps no state besides a device status word and
- *     the bound of its device-side waits.
+ *   - Every data pointer is a DEVICE pointer owned by the caller.  Besides a
+ *     device status word and the bound of its device-side waits, the library
+ *     keeps one buffer per (device, stream) for tokens whose key tiles are
+ *     split between two or more persistent clusters (their partial softmax
+ *     states are merged by the part that finishes last): ~40 MB on a GB300,
+ *     allocated by the first attention call on that stream and kept for the
+ *     life of the process.  A first call on a stream that is capturing a
+ *     CUDA graph allocates nothing and schedules whole tokens per cluster
+ *     instead (same results, less even load).  Calls on one stream share its
+ *     buffer in stream order; a captured graph uses the buffer of the stream
+ *     it was captured on and must not run concurrently with other calls on
+ *     that stream.
  *   - All tensors are dense row-major with the shapes given below.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream) and never synchronise.
@@ -38,8 +47,11 @@
  *     raises MLA_DEVICE_TIMEOUT.  Status bits accumulate until cleared; a
  *     later launch still runs in full.
  *   - Numerics: inputs bf16; products are exact; score and output
- *     accumulation in fp32 on the tensor cores (the two CTAs of a cluster
- *     work as one pair: each owns 64 of the 128 heads); the softmax weights P enter
+ *     accumulation in fp32 on the tensor cores (each CTA of a two-CTA
+ *     cluster owns half of the latent and rope dims; the two exchange fp32
+ *     partial scores, so both hold the same score tile); a token split
+ *     between clusters is merged in fp32 with the flash update's weights
+ *     2^(m_k - max m); the softmax weights P enter
  *     the P.V product as two bf16 terms, P_hi = bf16(p) and
  *     P_lo = bf16(p - P_hi), so their relative error stays below 2^-18; the
  *     values are the bf16 cache rows themselves; out is rounded to bf16 once.
@@ -204,6 +216,15 @@ mla_status mla_sparse_get_device_status(void* stream);
  * longer give up, which the tests use to exercise the timeout path.
  */
 mla_status mla_sparse_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * mla_sparse_launch_count -- number of kernel launches the attention entry
+ * points (mla_sparse_attn_fwd, mla_swa_fwd, mla_compressed_attn_fwd) have
+ * enqueued in this process so far, all threads and devices together.  One per
+ * call, two when a call cuts tokens between clusters (the attention kernel
+ * and the merge of the cut tokens' parts).  For accounting only.
+ */
+uint64_t mla_sparse_launch_count(void);
 
 /* ABI version of this header (major * 100 + minor). */
 int32_t mla_sparse_abi_version(void);

@@ -50,6 +50,7 @@
 #include <stdarg.h>
 #include <stdint.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <algorithm>
@@ -148,6 +149,11 @@ constexpr uint32_t kTmemRegion = 256;  // + 64 * (i % kRegions)
 constexpr uint32_t kTmemQ = 448;
 static_assert(kTmemRegion + 64 * kRegions <= kTmemQ && kTmemQ + 64 == kTmemCols, "TMEM layout");
 
+// Partial result of a cut token (one CTA rank's 256 latent dims): O as float4
+// units [(half * 32 + u) * 128 + h] (head h, dims 128 half + 4u .. + 3, so a
+// warp's 32 heads store 512 contiguous bytes), then m[128] and l[128].
+constexpr int kSlotFloats = kHeads * 256 + 2 * kHeads;
+
 __device__ unsigned int g_mla_status = 0;
 
 struct Params {
@@ -163,7 +169,15 @@ struct Params {
   float* lse;
   int S1, n_q, topk, num_blocks, mbps, n_tiles;
   int T;           // query tokens B * S1
-  int n_clusters;  // clusters in the grid; cluster c takes tokens c, c + n_clusters, ...
+  // Persistent clusters walk a stream of (token, tile) pairs.  Whole tokens:
+  // cluster c takes tokens c, c + n_clusters, ... (the tokens of one sequence
+  // run side by side on neighbouring clusters, so rows their lists share are
+  // read from HBM once).  Equal shares (list mode kModeListsCut): cluster c
+  // takes the tiles [c U / n_clusters, (c + 1) U / n_clusters) of
+  // g = t * n_tiles + i, U = T * n_tiles; a token cut between clusters leaves
+  // one partial softmax state per part in `ws`, merged by combine_kernel.
+  int n_clusters;
+  float* ws;  // equal shares: [n_clusters][2 segments][2 ranks] partial states (kSlotFloats each)
   int window;      // > 0: sliding window of this many positions instead of top-k lists
   // compressed cache (mode 2): entries after the window are compressed entries
   const void* cmp_nope;
@@ -181,16 +195,65 @@ struct Ctx {
   uint8_t* smem;
   uint32_t tmem;
   uint32_t crank;
-  int cid;    // cluster index
-  int ntok;   // tokens of this cluster
-  int total;  // key tiles of this cluster: ntok * n_tiles, one stream across its tokens
+  int cid;        // cluster index
+  int first;      // equal shares: tile g = t * n_tiles + i at the cluster's position 0 (T * n_tiles < 2^31)
+  int tok0;       // equal shares: the cluster's first token
+  int ntok;       // tokens of this cluster (with equal shares the first and last may be partial)
+  int total;      // key tiles of this cluster, one stream across its tokens
   uint64_t wait_ns;
   volatile uint32_t* abort;
   __device__ uint32_t bar(int i) const { return sbase + kOffBars + 8 * i; }
 };
 
+// Entry modes of the kernel: the token's top-k list (kModeLists, whole tokens
+// per cluster; kModeListsCut, equal shares of tiles), a sliding window of
+// positions (kModeWindow), or a window followed by compressed-cache entries
+// (kModeCompressed).  A compressed entry carries kCmpFlag through the index
+// and row rings.
+constexpr int kModeLists = 0;
+constexpr int kModeWindow = 1;
+constexpr int kModeCompressed = 2;
+constexpr int kModeListsCut = 3;
+constexpr int kCmpFlag = 1 << 30;
+__host__ __device__ constexpr bool lists_mode(int mode) { return mode == kModeLists || mode == kModeListsCut; }
+
 // Token of the m-th tile group of this cluster's stream.
-__device__ __forceinline__ int token_of(const Params& p, const Ctx& c, int m) { return c.cid + m * p.n_clusters; }
+template <int kMode>
+__device__ __forceinline__ int token_of(const Params& p, const Ctx& c, int m) {
+  if constexpr (kMode == kModeListsCut) return c.tok0 + m;
+  else return c.cid + m * p.n_clusters;
+}
+// Token of stream position jj, and the position's tile within that token.
+template <int kMode>
+__device__ __forceinline__ int token_at(const Params& p, const Ctx& c, int jj) {
+  if constexpr (kMode == kModeListsCut) return (c.first + jj) / p.n_tiles;
+  else return c.cid + (jj / p.n_tiles) * p.n_clusters;
+}
+template <int kMode>
+__device__ __forceinline__ int tile_at(const Params& p, const Ctx& c, int jj, int t) {
+  if constexpr (kMode == kModeListsCut) return c.first + jj - t * p.n_tiles;
+  else return jj % p.n_tiles;
+}
+// Stream positions [begin, end) of the cluster's m-th token.
+template <int kMode>
+__device__ __forceinline__ int seg_begin(const Params& p, const Ctx& c, int m) {
+  if constexpr (kMode == kModeListsCut) return max((c.tok0 + m) * p.n_tiles, c.first) - c.first;
+  else return m * p.n_tiles;
+}
+template <int kMode>
+__device__ __forceinline__ int seg_end(const Params& p, const Ctx& c, int m) {
+  if constexpr (kMode == kModeListsCut) return min((c.tok0 + m + 1) * p.n_tiles, c.first + c.total) - c.first;
+  else return (m + 1) * p.n_tiles;
+}
+// Equal shares: first tile of cluster cl, and the cluster whose range holds
+// tile g (the largest cl with start(cl) <= g).
+__device__ __forceinline__ int cluster_start(const Params& p, int cl) {
+  return static_cast<int>(static_cast<int64_t>(cl) * (p.T * p.n_tiles) / p.n_clusters);
+}
+__device__ __forceinline__ int cluster_of_tile(const Params& p, int g) {
+  const int64_t tiles = p.T * p.n_tiles;
+  return static_cast<int>((static_cast<int64_t>(g + 1) * p.n_clusters + tiles - 1) / tiles - 1);
+}
 
 __device__ __forceinline__ bool wait_bar(const Ctx& c, int idx, uint32_t parity) {
   return mbar_wait<false>(c.bar(idx), parity, c.abort, c.wait_ns);
@@ -237,18 +300,10 @@ __device__ __forceinline__ uint32_t xchg_offset(int h, int k) {
 static_assert(kIdxBatch == 4, "two entries per lane per tile, four tiles per pass");
 
 // Sequence of stream tile jj (jj < c.total).
+template <int kMode>
 __device__ __forceinline__ int seq_of_tile(const Params& p, const Ctx& c, int jj) {
-  return token_of(p, c, jj / p.n_tiles) / p.S1;
+  return token_at<kMode>(p, c, jj) / p.S1;
 }
-
-// Entry modes of the kernel: the token's top-k list (kModeLists), a sliding
-// window of positions (kModeWindow), or a window followed by compressed-cache
-// entries (kModeCompressed).  A compressed entry carries kCmpFlag through the
-// index and row rings.
-constexpr int kModeLists = 0;
-constexpr int kModeWindow = 1;
-constexpr int kModeCompressed = 2;
-constexpr int kCmpFlag = 1 << 30;
 
 // Entries of the pass starting at stream tile j0, -1 beyond the stream or the
 // list.  Lists: logical positions from topk_idx.  Window: the positions
@@ -263,10 +318,9 @@ __device__ __forceinline__ void index_load(const Params& p, const Ctx& c, int j0
 #pragma unroll
   for (int k = 0; k < kIdxBatch; ++k) {
     const int jj = j0 + k;
-    const int m = jj / p.n_tiles;
-    const int e0 = (jj - m * p.n_tiles) * kTileKeys + lane;
-    const int t = token_of(p, c, m);
-    if constexpr (kMode != kModeLists) {
+    const int t = token_at<kMode>(p, c, jj);
+    const int e0 = tile_at<kMode>(p, c, jj, t) * kTileKeys + lane;
+    if constexpr (!lists_mode(kMode)) {
       const int b = t / p.S1;
       const int pos = (jj < c.total ? __ldg(p.act_seqs + b) : 0) - p.S1 + (t - b * p.S1);
       const int first = pos - p.window + 1;
@@ -305,9 +359,9 @@ __device__ void index_role(const Params& p, const Ctx& c, int iw, int lane, int 
   // pull the cluster's top-k rows and their sequences' block-table rows towards
   // L2 up front (one 128-byte line per prefetch; the warps split the lines)
   for (int m = 0; m < c.ntok; ++m) {
-    const int t = token_of(p, c, m);
+    const int t = token_of<kMode>(p, c, m);
     const int32_t* bt = p.block_table + static_cast<int64_t>(t / p.S1) * p.mbps;
-    if constexpr (kMode == kModeLists) {  // only list mode reads topk_idx
+    if constexpr (lists_mode(kMode)) {  // only list modes read topk_idx
       const int32_t* tk = p.topk_idx + static_cast<int64_t>(t) * p.topk;
       for (int e = (iw * 32 + lane) * 32; e < p.topk + 32; e += kIndexWarps * 32 * 32)
         prefetch_l2(tk + min(e, p.topk - 1));
@@ -328,12 +382,12 @@ __device__ void index_role(const Params& p, const Ctx& c, int iw, int lane, int 
         const int mb = cmp ? p.cmp_mbps : p.mbps;
         const int32_t* bt = cmp ? p.cmp_block_table : p.block_table;
         blk[q] = (idx[q] >= 0 && slot < mb)
-                     ? __ldg(bt + static_cast<int64_t>(seq_of_tile(p, c, j0 + (q >> 1))) * mb + slot)
+                     ? __ldg(bt + static_cast<int64_t>(seq_of_tile<kMode>(p, c, j0 + (q >> 1))) * mb + slot)
                      : -1;
       } else {
         const int slot = idx[q] >> 7;
         blk[q] = (idx[q] >= 0 && slot < p.mbps)
-                     ? __ldg(p.block_table + static_cast<int64_t>(seq_of_tile(p, c, j0 + (q >> 1))) * p.mbps + slot)
+                     ? __ldg(p.block_table + static_cast<int64_t>(seq_of_tile<kMode>(p, c, j0 + (q >> 1))) * p.mbps + slot)
                      : -1;
       }
     }
@@ -348,7 +402,7 @@ __device__ void index_role(const Params& p, const Ctx& c, int iw, int lane, int 
 #pragma unroll
     for (int k = 0; k < kIdxBatch; ++k) {
       if (k >= nb) continue;
-      const int act = __ldg(p.act_seqs + seq_of_tile(p, c, j0 + k));
+      const int act = __ldg(p.act_seqs + seq_of_tile<kMode>(p, c, j0 + k));
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int q = 2 * k + u;
@@ -585,11 +639,13 @@ __device__ __forceinline__ void issue_pv(const Ctx& c, int i, bool first_of_toke
 // last S of a token is followed by a commit to QFree (its Q may then be
 // replaced), and the first P.V of token m > 0 waits until O of token m - 1 has
 // been read out (OFree phase m - 1) and starts a fresh accumulator.
+template <int kMode>
 __device__ void mma_role(const Params& p, const Ctx& c) {
   bool ok = true;
   int ks = 0, kp = 0;
-  int s_tok = 0, s_in = 0;  // token ordinal and tile-in-token of ks
+  int s_tok = 0, s_in = 0;  // token ordinal and tile-in-segment of ks
   int p_tok = 0, p_in = 0;  // the same for kp
+  int s_len = seg_end<kMode>(p, c, 0) - seg_begin<kMode>(p, c, 0), p_len = s_len;  // tiles of the token's segment
   bool s_q = false;         // Q of token s_tok seen ready
   uint64_t t_idle = 0;
   uint32_t spins = 0;
@@ -599,9 +655,10 @@ __device__ void mma_role(const Params& p, const Ctx& c) {
         (p_in != 0 || p_tok == 0 || mbar_poll(c.bar(kBarOFree), (p_tok - 1) & 1))) {
       issue_pv(c, kp, p_in == 0);
       ++kp;
-      if (++p_in == p.n_tiles) {
+      if (++p_in == p_len) {
         p_in = 0;
         ++p_tok;
+        p_len = seg_end<kMode>(p, c, p_tok) - seg_begin<kMode>(p, c, p_tok);
       }
       progressed = true;
     }
@@ -611,10 +668,11 @@ __device__ void mma_role(const Params& p, const Ctx& c) {
           (ks < kRegions || mbar_poll(c.bar(kBarPvDone + ks % kRegions), ((ks / kRegions) & 1) ^ 1))) {
         issue_s(c, ks);
         ++ks;
-        if (++s_in == p.n_tiles) {
+        if (++s_in == s_len) {
           umma_commit(c.bar(kBarQFree));  // the token's score MMAs: its Q may be replaced
           s_in = 0;
           ++s_tok;
+          s_len = seg_end<kMode>(p, c, s_tok) - seg_begin<kMode>(p, c, s_tok);
           s_q = false;
         }
         progressed = true;
@@ -684,10 +742,115 @@ __device__ __forceinline__ void load_q(const Params& p, const Ctx& c, int h, int
   }
 }
 
+// ------------------------------------------------------------------ cut tokens
+// With equal shares, a token's tiles may be cut between consecutive clusters.
+// Each part ends with its own online softmax state: O relative to its running
+// max m (log2 units) and its row sum l.  The parts combine exactly as in the
+// flash update: with M = max m_k and w_k = 2^(m_k - M),
+// O = sum w_k O_k / sum w_k l_k and lse = M + log2(sum w_k l_k).
+
+// Slot of the part of token t computed by cluster cl, CTA rank r: segment 0
+// holds the cluster's first token, segment 1 its last (a cut token is one of
+// the two).
+__device__ __forceinline__ float* part_slot(const Params& p, int cl, int t, uint32_t r) {
+  const int seg = t == cluster_start(p, cl) / p.n_tiles ? 0 : 1;
+  return p.ws + (static_cast<int64_t>(cl * 2 + seg) * 2 + r) * kSlotFloats;
+}
+
+// Store this cluster's part of cut token t (O in TMEM at tO, m, l_tot), then
+// release O for the next token.  The TMEM loads are warp-wide; only live
+// heads store.
+__device__ __noinline__ void store_part(const Params& p, const Ctx& c, int t, int h, int half, bool live, uint32_t tO,
+                                        float m, float l_tot) {
+  float* own = part_slot(p, c.cid, t, c.crank);
+  float4* so = reinterpret_cast<float4*>(own) + half * 32 * kHeads + h;
+#pragma unroll 1
+  for (int ch = 0; ch < 4; ++ch) {
+    uint32_t o[32];
+    tmem_ld_32x32b_x32(tO + 32 * ch, o);
+    tmem_wait_ld();
+    if (live) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        so[(ch * 8 + k) * kHeads] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
+                                                __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
+    }
+  }
+  if (live && half == 0) {
+    own[kHeads * 256 + h] = m;
+    own[kHeads * 256 + kHeads + h] = l_tot;
+  }
+  tc_fence_before();
+  mbar_arrive(c.bar(kBarOFree));
+}
+
+// One block per (token, CTA rank, 8 of the rank's 256 latent dims), one thread
+// per head: merges the parts of a cut token in one pass, with the running
+// maximum of the flash update (tokens that are not cut return at once).  The
+// parts are read eight at a time so that their loads are in flight together.
+// Runs after the attention kernel on the same stream.
+constexpr int kCombineDims = 8;
+constexpr int kCombineParts = 8;
+__global__ void __launch_bounds__(kHeads) combine_kernel(const __grid_constant__ Params p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the attention kernel's stores are visible
+  const int t = blockIdx.x, r = blockIdx.y, ch = blockIdx.z, h = threadIdx.x;
+  const int g0 = t * p.n_tiles;
+  const int c_first = cluster_of_tile(p, g0), c_last = cluster_of_tile(p, g0 + p.n_tiles - 1);
+  if (c_first == c_last || h >= p.n_q) return;
+  // dims [8 ch, 8 ch + 8) of the rank: column half ch / 16, float4 units (ch % 16) * 2 + {0, 1}
+  const int unit0 = ((ch >> 4) * 32 + (ch & 15) * 2) * kHeads + h;
+  float mx = -INFINITY, lsum = 0.f, acc[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+  for (int base = c_first; base <= c_last; base += kCombineParts) {
+    float mk[kCombineParts], lk[kCombineParts];
+    float4 v[kCombineParts][2];
+#pragma unroll
+    for (int u = 0; u < kCombineParts; ++u) {
+      const bool in = base + u <= c_last;
+      const float* sl = part_slot(p, in ? base + u : c_last, t, r);
+      mk[u] = in ? __ldcg(sl + kHeads * 256 + h) : -INFINITY;
+      lk[u] = in ? __ldcg(sl + kHeads * 256 + kHeads + h) : 0.f;
+      const float4* src = reinterpret_cast<const float4*>(sl) + unit0;
+      v[u][0] = in ? __ldcg(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[u][1] = in ? __ldcg(src + kHeads) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kCombineParts; ++u) {
+      if (mk[u] == -INFINITY) continue;  // a part without a valid key adds nothing
+      if (mk[u] > mx) {
+        const float f = mx == -INFINITY ? 0.f : exp2f(mx - mk[u]);
+        lsum *= f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[k] *= f;
+        mx = mk[u];
+      }
+      const float w = exp2f(mk[u] - mx);
+      lsum = fmaf(w, lk[u], lsum);
+      acc[0] = fmaf(w, v[u][0].x, acc[0]);
+      acc[1] = fmaf(w, v[u][0].y, acc[1]);
+      acc[2] = fmaf(w, v[u][0].z, acc[2]);
+      acc[3] = fmaf(w, v[u][0].w, acc[3]);
+      acc[4] = fmaf(w, v[u][1].x, acc[4]);
+      acc[5] = fmaf(w, v[u][1].y, acc[5]);
+      acc[6] = fmaf(w, v[u][1].z, acc[6]);
+      acc[7] = fmaf(w, v[u][1].w, acc[7]);
+    }
+  }
+  const float inv_l = lsum > 0.f ? 1.f / lsum : 0.f;
+  const int64_t qrow = static_cast<int64_t>(t) * p.n_q + h;
+  *reinterpret_cast<uint4*>(p.out + qrow * 512 + r * 256 + ch * kCombineDims) =
+      make_uint4(pack_bf16x2(acc[0] * inv_l, acc[1] * inv_l), pack_bf16x2(acc[2] * inv_l, acc[3] * inv_l),
+                 pack_bf16x2(acc[4] * inv_l, acc[5] * inv_l), pack_bf16x2(acc[6] * inv_l, acc[7] * inv_l));
+  if (r == 0 && ch == 0 && p.lse != nullptr)
+    p.lse[qrow] = lsum > 0.f ? (mx + log2f(lsum)) * 0.69314718055994530942f : -INFINITY;
+}
+
 // The cluster's tokens in order.  Before the epilogue of token m the warps load
 // Q of token m + 1 (once QFree says the score MMAs of token m are complete),
 // so the next token's first score tiles are computed while O of token m is
 // read out; after reading O they arrive on OFree.
+template <int kMode>
 __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) {
   const int q = warp & 3;          // TMEM lane quadrant
   const int half = warp >> 2;      // key columns [32 half, 32 half + 32)
@@ -697,7 +860,7 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
   const uint32_t tO = c.tmem + lane_off + kTmemO + 128 * half;
   const uint32_t tQ = c.tmem + lane_off + kTmemQ;
   const bool live = h < p.n_q;
-  load_q(p, c, h, half, live, static_cast<int64_t>(token_of(p, c, 0)) * p.n_q + h, tQ);
+  load_q(p, c, h, half, live, static_cast<int64_t>(token_of<kMode>(p, c, 0)) * p.n_q + h, tQ);
   const uint32_t peer = c.crank ^ 1u;
   const uint32_t dep_zero = *reinterpret_cast<volatile uint32_t*>(c.smem + kOffZero);
   float* pair = reinterpret_cast<float*>(c.smem + kOffPair);
@@ -708,13 +871,13 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
   // score is scaled first and mul = 1
   const bool raw_max = scl > 0.f;
   const float mul = raw_max ? scl : 1.f;
-  int pa = 0;  // uses of the row-max / row-sum pair barrier so far (its phase)
+  int pa = 0;    // uses of the row-max / row-sum pair barrier so far (its phase)
   for (int mt = 0; mt < c.ntok; ++mt) {
-    const int64_t qrow = static_cast<int64_t>(token_of(p, c, mt)) * p.n_q + h;
+    const int64_t qrow = static_cast<int64_t>(token_of<kMode>(p, c, mt)) * p.n_q + h;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int i = 0; i < p.n_tiles; ++i) {
-      const int j = mt * p.n_tiles + i;  // position in the cluster's tile stream
+    const int jb = seg_begin<kMode>(p, c, mt), je = seg_end<kMode>(p, c, mt);
+    for (int j = jb; j < je; ++j) {  // positions in the cluster's tile stream
       {
         // own partial score tile i, read out at once so the next score MMA can
         // start while the peer's partial is still on its way
@@ -778,7 +941,7 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
           l *= f;
           m = mx;
         }
-        if (__any_sync(0xffffffffu, grow) && i > 0) {
+        if (__any_sync(0xffffffffu, grow) && j > jb) {
           // O may only be rescaled once P(j-1).V has been accumulated into it
           if (!warp_wait(c, kBarPvDone + (j - 1) % kRegions, ((j - 1) / kRegions) & 1)) { ok = false; break; }
           tc_fence_after();
@@ -825,7 +988,7 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
       // the next token's Q replaces this one's once its score MMAs are complete
       if (!warp_wait(c, kBarQFree, mt & 1)) return;
       tc_fence_after();
-      load_q(p, c, h, half, live, static_cast<int64_t>(token_of(p, c, mt + 1)) * p.n_q + h, tQ);
+      load_q(p, c, h, half, live, static_cast<int64_t>(token_of<kMode>(p, c, mt + 1)) * p.n_q + h, tQ);
     }
     // l over the whole row: add the partner's column half (same order in both threads)
     float* slot_l = pair + (pa & 1) * 2 * kHeads;
@@ -834,9 +997,16 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
     if (!warp_wait(c, kBarPairA + q, pa & 1)) return;
     ++pa;
     const float l_tot = half == 0 ? l + slot_l[kHeads + h] : slot_l[h] + l;
-    const int jl = (mt + 1) * p.n_tiles - 1;  // the token's last tile
+    const int jl = je - 1;  // the segment's last tile
     if (!warp_wait(c, kBarPvDone + jl % kRegions, (jl / kRegions) & 1)) return;
     tc_fence_after();
+    if constexpr (kMode == kModeListsCut) {
+      if (je - jb < p.n_tiles) {
+        // the token's tiles are cut between clusters: store this part's state
+        store_part(p, c, token_of<kMode>(p, c, mt), h, half, live, tO, m, l_tot);
+        continue;
+      }
+    }
     const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
     uint4* op = reinterpret_cast<uint4*>(p.out + qrow * 512 + c.crank * 256 + half * 128);
 #pragma unroll 1
@@ -876,8 +1046,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_spa
   c.sbase = smem_u32(smem);
   c.crank = cluster_ctarank();
   c.cid = blockIdx.x >> 1;
-  c.ntok = (p.T - c.cid + p.n_clusters - 1) / p.n_clusters;
-  c.total = c.ntok * p.n_tiles;
+  if constexpr (kMode == kModeListsCut) {
+    c.first = cluster_start(p, c.cid);
+    c.total = cluster_start(p, c.cid + 1) - c.first;
+    c.tok0 = c.first / p.n_tiles;
+    c.ntok = (c.first + c.total - 1) / p.n_tiles - c.tok0 + 1;
+  } else {
+    c.first = 0;
+    c.tok0 = c.cid;
+    c.ntok = (p.T - c.cid + p.n_clusters - 1) / p.n_clusters;
+    c.total = c.ntok * p.n_tiles;
+  }
   c.abort = reinterpret_cast<volatile uint32_t*>(smem + kOffAbort);
   c.wait_ns = p.wait_ns;
   if (tid == 0) {
@@ -929,7 +1108,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_spa
 
   if (warp < kSenderWarp0) {
     regs_increase<Regs<kInt8>::kSoftmax>();
-    if (!*c.abort) softmax_role(p, c, warp, lane);
+    if (!*c.abort) softmax_role<kMode>(p, c, warp, lane);
   } else if (warp < kGatherWarp0) {
     if (!*c.abort) sender_role(p, c, warp - kSenderWarp0, lane);
   } else if (warp < kMmaWarp) {
@@ -939,7 +1118,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_spa
     regs_decrease<Regs<kInt8>::kControl>();
     if (!*c.abort) {
       if (warp == kMmaWarp) {
-        if (lane == 0) mma_role(p, c);
+        if (lane == 0) mma_role<kMode>(p, c);
         __syncwarp();
       } else if (warp < kIndexWarp + kIndexWarps) {
         index_role<kMode>(p, c, warp - kIndexWarp, lane, idx0);
@@ -976,10 +1155,64 @@ mla_status fail(mla_status s, const char* fmt, ...) {
 bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0; }
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_attr_once[kMaxDevices][6];
-cudaError_t g_attr_err[kMaxDevices][6];
+// kernel variants: kv = int8 + 2 * mode (mode kModeLists .. kModeListsCut)
+constexpr int kVariants = 8;
+std::once_flag g_attr_once[kMaxDevices][kVariants];
+cudaError_t g_attr_err[kMaxDevices][kVariants];
 
-int g_max_clusters[kMaxDevices][6];
+int g_max_clusters[kMaxDevices][kVariants];
+
+// Per (device, stream) buffer for the partial softmax states of cut tokens:
+// one slot per (cluster, first/last token, CTA rank).  Allocated by the first
+// call on a stream that cuts tokens (not under graph capture) and kept for the
+// life of the process.
+struct CutBuffer {
+  int dev;
+  void* stream;
+  float* ws;
+  int clusters;
+};
+std::mutex g_cut_mu;
+CutBuffer* g_cut = nullptr;
+int g_cut_n = 0, g_cut_cap = 0;
+
+// The buffer for (dev, stream), or nullptr when there is none and none may be
+// made now (the stream is capturing a graph) or the allocation failed (*err).
+float* cut_buffer(int dev, cudaStream_t stream, int clusters, cudaError_t* err) {
+  std::lock_guard<std::mutex> lock(g_cut_mu);
+  *err = cudaSuccess;
+  for (int i = 0; i < g_cut_n; ++i) {
+    const CutBuffer& b = g_cut[i];
+    if (b.dev == dev && b.stream == static_cast<void*>(stream) && b.clusters >= clusters) return b.ws;
+  }
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return nullptr;
+  if (g_cut_n == g_cut_cap) {
+    const int cap = g_cut_cap ? 2 * g_cut_cap : 8;
+    CutBuffer* nb = static_cast<CutBuffer*>(realloc(g_cut, sizeof(CutBuffer) * cap));
+    if (nb == nullptr) return nullptr;
+    g_cut = nb;
+    g_cut_cap = cap;
+  }
+  void* mem = nullptr;
+  const cudaError_t e = cudaMalloc(&mem, static_cast<size_t>(clusters) * 4 * mlasp::kSlotFloats * sizeof(float));
+  if (e != cudaSuccess) {
+    *err = e;
+    return nullptr;
+  }
+  CutBuffer& b = g_cut[g_cut_n++];
+  b.dev = dev;
+  b.stream = static_cast<void*>(stream);
+  b.ws = static_cast<float*>(mem);
+  b.clusters = clusters;
+  return b.ws;
+}
+
+// Equal shares give each cluster at least this many tiles.
+constexpr int64_t kMinPartTiles = 2;
+
+// Kernel launches enqueued by the attention entry points.
+std::atomic<unsigned long long> g_launches{0};
 
 // Bound of every device-side wait of the next launches (nanoseconds).
 std::atomic<unsigned long long> g_wait_ns{500ull * 1000ull * 1000ull};
@@ -1027,7 +1260,7 @@ cudaError_t prepare_kernel(int dev) {
 
 extern "C" {
 
-int32_t mla_sparse_abi_version(void) { return 200; }
+int32_t mla_sparse_abi_version(void) { return 201; }
 
 const char* mla_sparse_last_error(void) { return g_last_error; }
 
@@ -1097,7 +1330,7 @@ mla_status attn_fwd(const mla_dims* dims, const void* q_nope, const void* q_rope
   if (dev < 0 || dev >= kMaxDevices) return fail(MLA_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
   const bool int8 = d.kv_dtype == MLA_KV_INT8;
   const int kmode = cmp != nullptr ? mlasp::kModeCompressed : (window > 0 ? mlasp::kModeWindow : mlasp::kModeLists);
-  const int kv = (int8 ? 1 : 0) + 2 * kmode;
+  int kv = (int8 ? 1 : 0) + 2 * kmode;
   switch (kv) {
     case 0: e = prepare_kernel<false, mlasp::kModeLists>(dev); break;
     case 1: e = prepare_kernel<true, mlasp::kModeLists>(dev); break;
@@ -1127,11 +1360,34 @@ mla_status attn_fwd(const mla_dims* dims, const void* q_nope, const void* q_rope
   p.n_tiles = (d.topk + mlasp::kTileKeys - 1) / mlasp::kTileKeys;
   p.scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634);
   p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
-  // persistent clusters: as many as run at once (never more than tokens); cluster
-  // c takes tokens c, c + n_clusters, ... as one stream of key tiles
+  // Persistent clusters, as many as run at once.  Whole tokens per cluster by
+  // default.  Equal shares of tiles (list mode only) cost a token switch per
+  // cut, a merge launch and the L2 sharing between a sequence's tokens; they
+  // are taken when whole tokens would leave the longest cluster at least
+  // twice the equal share (few tokens with long lists, most clusters idle).
   const int max_clusters = g_max_clusters[dev][kv];
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   p.T = static_cast<int>(T);
+  const int64_t tiles = T * p.n_tiles;
+  if (tiles >= (1ll << 31) - p.n_tiles)
+    return fail(MLA_ERR_SHAPE, "B*S1 x key tiles per token = %lld too large", static_cast<long long>(tiles));
+  p.ws = nullptr;
   p.n_clusters = static_cast<int>(T < max_clusters ? T : max_clusters);
+  if (kmode == mlasp::kModeLists) {
+    const int64_t nc_equal = std::min<int64_t>(max_clusters, std::max<int64_t>(1, tiles / kMinPartTiles));
+    const int64_t most_whole = (T + p.n_clusters - 1) / p.n_clusters * p.n_tiles;
+    const int64_t most_equal = (tiles + nc_equal - 1) / nc_equal;
+    if (most_whole >= 2 * most_equal && most_whole >= 4) {
+      p.ws = cut_buffer(dev, s, max_clusters, &e);
+      if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "buffer for cut tokens: %s", cudaGetErrorString(e));
+      if (p.ws != nullptr) {
+        e = int8 ? prepare_kernel<true, mlasp::kModeListsCut>(dev) : prepare_kernel<false, mlasp::kModeListsCut>(dev);
+        if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "kernel set-up: %s", cudaGetErrorString(e));
+        kv = (int8 ? 1 : 0) + 2 * mlasp::kModeListsCut;
+        p.n_clusters = static_cast<int>(std::min<int64_t>(nc_equal, g_max_clusters[dev][kv]));
+      }
+    }
+  }
   p.window = window;
   p.cmp_nope = cmp ? cmp->nope : nullptr;
   p.cmp_rope = cmp ? static_cast<const uint16_t*>(cmp->rope) : nullptr;
@@ -1143,17 +1399,35 @@ mla_status attn_fwd(const mla_dims* dims, const void* q_nope, const void* q_rope
   p.cmp_ratio = cmp ? cmp->ratio : 1;
   p.cmp_topk = cmp_slots;
   const dim3 grid(static_cast<unsigned>(2 * p.n_clusters));
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   switch (kv) {
     case 0: mlasp::mla_sparse_fwd_kernel<false, mlasp::kModeLists><<<grid, mlasp::kThreads, mlasp::kSmemBytes, s>>>(p); break;
     case 1: mlasp::mla_sparse_fwd_kernel<true, mlasp::kModeLists><<<grid, mlasp::kThreads, mlasp::kSmemBytes, s>>>(p); break;
     case 2: mlasp::mla_sparse_fwd_kernel<false, mlasp::kModeWindow><<<grid, mlasp::kThreads, mlasp::kSmemBytes, s>>>(p); break;
     case 3: mlasp::mla_sparse_fwd_kernel<true, mlasp::kModeWindow><<<grid, mlasp::kThreads, mlasp::kSmemBytes, s>>>(p); break;
     case 4: mlasp::mla_sparse_fwd_kernel<false, mlasp::kModeCompressed><<<grid, mlasp::kThreads, mlasp::kSmemBytes, s>>>(p); break;
-    default: mlasp::mla_sparse_fwd_kernel<true, mlasp::kModeCompressed><<<grid, mlasp::kThreads, mlasp::kSmemBytes, s>>>(p); break;
+    case 5: mlasp::mla_sparse_fwd_kernel<true, mlasp::kModeCompressed><<<grid, mlasp::kThreads, mlasp::kSmemBytes, s>>>(p); break;
+    case 6: mlasp::mla_sparse_fwd_kernel<false, mlasp::kModeListsCut><<<grid, mlasp::kThreads, mlasp::kSmemBytes, s>>>(p); break;
+    default: mlasp::mla_sparse_fwd_kernel<true, mlasp::kModeListsCut><<<grid, mlasp::kThreads, mlasp::kSmemBytes, s>>>(p); break;
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (p.ws != nullptr) {
+    // merge the cut tokens' parts; launched early, it waits for the kernel above
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(T), 2, 256 / mlasp::kCombineDims);
+    cfg.blockDim = dim3(mlasp::kHeads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, mlasp::combine_kernel, p);
+    if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "merge launch: %s", cudaGetErrorString(e));
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+  }
   return MLA_OK;
 }
 
@@ -1203,6 +1477,8 @@ mla_status mla_sparse_set_wait_limit_ns(uint64_t ns) {
 }
 
 mla_status mla_sparse_get_device_status(void* stream) { return mla_sparse_device_status(stream, nullptr, 0); }
+
+uint64_t mla_sparse_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 mla_status mla_sparse_device_status(void* stream, uint32_t* flags, int32_t clear) {
   g_last_error[0] = '\0';

@@ -192,7 +192,7 @@ def test_deterministic_and_permutation_stable():
 # workloads are checked on every token; the 4096-token prefill on 274 tokens,
 # every 15th one plus the last (15 is prime to the number of clusters, so the
 # sample covers every cluster and many stream positions).
-@pytest.mark.parametrize("name", ["mtp_decode", "int8_decode", "varlen_decode"])
+@pytest.mark.parametrize("name", ["mtp_decode", "int8_decode", "varlen_decode", "mtp_decode_b2"])
 def test_full_size_decode_every_token(name):
     inp = workloads.NAMED[name]()
     T = inp["dims"]["B"] * inp["dims"]["S1"]

@@ -22,10 +22,15 @@ torch = pytest.importorskip("torch")
 from gpu_util import assert_lse_close, assert_out_close, launch, run_gpu, to_device  # noqa: E402
 
 
-@pytest.mark.parametrize("name, kv_int8", [("mtp", False), ("mtp", True), ("swa", False)])
-def test_a_wait_that_runs_out_is_reported_and_the_next_call_is_exact(name, kv_int8):
+# B=64 S1=2 runs whole tokens per cluster; B=15 S1=2 (30 tokens of 32 tiles)
+# cuts tokens between clusters, so a launch that gives up leaves arrival
+# counts behind that the next launch must ignore.
+@pytest.mark.parametrize("name, B, topk, kv_int8", [("mtp", 64, 512, False), ("mtp", 64, 512, True),
+                                                    ("mtp", 15, 2048, False), ("swa", 64, 512, False)])
+def test_a_wait_that_runs_out_is_reported_and_the_next_call_is_exact(name, B, topk, kv_int8):
     import mla_sparse_top_gb300 as mla
-    inp = workloads.make_inputs(B=3, S1=2, n_q=128, act_seqs=[4000, 2500, 700], topk=512, seed=70,
+    acts = [4000, 2500, 700, 8000]
+    inp = workloads.make_inputs(B=B, S1=2, n_q=128, act_seqs=[acts[b % 4] for b in range(B)], topk=topk, seed=70,
                                 kv_int8=kv_int8)
     dev = to_device(inp)
     assert mla.device_status(clear=True) == 0
@@ -45,6 +50,6 @@ def test_a_wait_that_runs_out_is_reported_and_the_next_call_is_exact(name, kv_in
     out, lse, status = run_gpu(inp, dev=dev)
     assert status == 0, f"status {status:#x} after the bound was restored"
     ref_out, ref_lse, _ = oracle.forward(inp)
-    assert_out_close(out, ref_out, f"{name} int8={kv_int8} after a timeout")
-    assert_lse_close(lse, ref_lse, f"{name} int8={kv_int8} after a timeout")
+    assert_out_close(out, ref_out, f"{name} B={B} int8={kv_int8} after a timeout")
+    assert_lse_close(lse, ref_lse, f"{name} B={B} int8={kv_int8} after a timeout")
     assert np.isfinite(out).all()

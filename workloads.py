@@ -152,6 +152,11 @@ def mtp_decode(seed: int = 1, B: int = 64) -> dict:
     return make_inputs(B=B, S1=2, n_q=128, act_seqs=[8192] * B, topk=2048, seed=seed, name="mtp_decode")
 
 
+def mtp_decode_b2(seed: int = 16) -> dict:
+    """Low-batch MTP decode: B=2 S1=2 (4 query tokens), otherwise as mtp_decode."""
+    return make_inputs(B=2, S1=2, n_q=128, act_seqs=[8192] * 2, topk=2048, seed=seed, name="mtp_decode_b2")
+
+
 def int8_decode(seed: int = 2, B: int = 64) -> dict:
     """As mtp_decode with key_nope INT8 per 128-group (scale = absmax/127)."""
     return make_inputs(B=B, S1=2, n_q=128, act_seqs=[8192] * B, topk=2048, seed=seed, kv_int8=True,
@@ -185,6 +190,7 @@ def prefill(seed: int = 4, B: int = 4, S1: int = 1024) -> dict:
 NAMED = {
     "tiny_decode": tiny_decode,
     "mtp_decode": mtp_decode,
+    "mtp_decode_b2": mtp_decode_b2,
     "int8_decode": int8_decode,
     "varlen_decode": varlen_decode,
     "prefill": prefill,

@@ -22,16 +22,18 @@
  * Conventions
  *   - Every data pointer is a DEVICE pointer owned by the caller.  Besides a
  *     device status word and the bound of its device-side waits, the library
- *     keeps one buffer per (device, stream) for tokens whose key tiles are
- *     split between two or more persistent clusters (their partial softmax
- *     states are merged by the part that finishes last): ~40 MB on a GB300,
- *     allocated by the first attention call on that stream and kept for the
- *     life of the process.  A first call on a stream that is capturing a
- *     CUDA graph allocates nothing and schedules whole tokens per cluster
- *     instead (same results, less even load).  Calls on one stream share its
- *     buffer in stream order; a captured graph uses the buffer of the stream
- *     it was captured on and must not run concurrently with other calls on
- *     that stream.
+ *     keeps one buffer per (device, stream) for calls with few tokens and long
+ *     lists (whole tokens per cluster would leave the longest cluster at least
+ *     twice an equal share of the key tiles): such a call gives every cluster
+ *     an equal share, a token cut between clusters leaves one partial softmax
+ *     state per part in the buffer, and a second launch merges them.  The
+ *     buffer (~40 MB on a GB300) is allocated by the first such call on the
+ *     stream and kept for the life of the process.  A first such call on a
+ *     stream that is capturing a CUDA graph allocates nothing and schedules
+ *     whole tokens instead (same results, less even load).  Calls on one
+ *     stream share its buffer in stream order; a captured graph uses the
+ *     buffer of the stream it was captured on and must not run concurrently
+ *     with other calls on that stream.
  *   - All tensors are dense row-major with the shapes given below.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream) and never synchronise.
@@ -49,7 +51,7 @@
  *   - Numerics: inputs bf16; products are exact; score and output
  *     accumulation in fp32 on the tensor cores (each CTA of a two-CTA
  *     cluster owns half of the latent and rope dims; the two exchange fp32
- *     partial scores, so both hold the same score tile); a token split
+ *     partial scores, so both hold the same score tile); a token cut
  *     between clusters is merged in fp32 with the flash update's weights
  *     2^(m_k - max m); the softmax weights P enter
  *     the P.V product as two bf16 terms, P_hi = bf16(p) and

@@ -15,8 +15,8 @@ selection kernel as a programmatic dependent launch).
 cache writer (128 / 4096 new rows quantised into an INT8 cache of 4096 blocks).
 ``--workload prolog_decode`` / ``prolog_prefill`` time the MLA Prolog (128 /
 1000 tokens, hidden 7168, q_lora 1536, 128 heads, random-init weights): one
-step = one mla_prolog call (seven launches of the library's kernels: three of
-its tcgen05 product kernel, the partial-sum reduction and three row kernels).
+step = one mla_prolog call (five launches of the library's kernels: three of
+its tcgen05 product kernel and two row kernels).
 
 Prints one JSON line (rank 0).  ``value`` is microseconds per call (the
 device-timed kernel, CUDA events on the launching stream, L2 flushed by a
@@ -1120,13 +1120,12 @@ def main_prolog(args, world, rank, local_rank):
                          "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                          else "fallback",
                          "algorithmic_bytes_per_launch": nbytes,
-                         "kernel": "the whole mla_prolog call (gemm_kernel x3 + sum_slots_kernel, kv_rows_kernel, "
-                                   "cq_rows_kernel, q_heads_kernel)",
+                         "kernel": "the whole mla_prolog call (gemm_kernel x3 + x_rows_kernel, q_heads_kernel)",
                          "tensor_tflops": round(flops / (us * 1e-6) / 1e12, 1),
                          "tensor_frac_of_bf16_peak": round(flops / (us * 1e-6) / 1e12 / bf16_tf, 4)},
             "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h)},
-            "gpu_launches": 7 * args.steps, "clocks": clock_summary,
+            "gpu_launches": 5 * args.steps, "clocks": clock_summary,
             "device_status": status,
         }
         if not args.no_cpu_baseline:

@@ -35,7 +35,7 @@
  * library's kernels: the four matrix products in its tcgen05 product kernel
  * (the weights streamed by TMA as the MMA's A operand, x @ wq_a and x @ wkv
  * in one launch), the norms, rotations and the cache write in its row
- * kernels; all six launches go to `stream`, so the call is capturable into a
+ * kernels; all five launches go to `stream`, so the call is capturable into a
  * CUDA graph.  The first call on each device sets the product kernel's
  * shared-memory attribute and looks up the driver's tensor-map encoder: make
  * it before any stream capture begins.
@@ -88,9 +88,10 @@ size_t mla_prolog_workspace_bytes(const mla_prolog_dims* dims);
  * kv_rope     bf16 [num_rows, 64], updated in place
  * kv_scales   fp32 [num_rows, 4] (INT8 only; NULL for bf16), updated in place
  * workspace   >= mla_prolog_workspace_bytes(dims) bytes, 256-byte aligned
- * Every pointer 16-byte aligned (cache_index 8-byte).  Seven launches (the
- * key projection and the key-row kernel on the internal second stream) and
- * two event records; MLA_ERR_SHAPE when the workspace is too small.
+ * Every pointer 16-byte aligned (cache_index 8-byte).  Five launches on
+ * `stream` (the two x projections, the c^Q and key rows, c^Q @ wq_b, the
+ * per-head norms, the absorption), each a programmatic dependent of the
+ * previous one; MLA_ERR_SHAPE when the workspace is too small.
  */
 mla_status mla_prolog(const mla_prolog_dims* dims, const void* x, const mla_prolog_weights* w, const float* cos,
                       const float* sin, const int64_t* cache_index, void* q_nope, void* q_rope, void* kv_nope,

@@ -8,14 +8,14 @@
 // section MLA Prolog (weight absorption in decode: the query's no-position
 // part is taken into the 512-wide latent space by w_uk).
 //
-// Data flow per call (T tokens, H heads), six launches on the caller's stream:
+// Data flow per call (T tokens, H heads), five launches on the caller's stream:
 //   gemm_kernel   c_raw = x @ wq_a and kv_raw = x @ wkv in one launch (the
 //                 page runs the two projections side by side), fp32 partial
 //                 sums over k splits in separate slots
-//   kv_rows_kernel  k = RMSNorm(sum of kv_raw slots) * gamma_ckv, RoPE on
-//                 k[512:], rounded to bf16 and written (bf16 or INT8) into
-//                 the cache row
-//   cq_rows_kernel  c^Q = bf16(RMSNorm(sum of c_raw slots) * gamma_cq)
+//   x_rows_kernel one block per token: c^Q = bf16(RMSNorm(sum of c_raw
+//                 slots) * gamma_cq) by four warps; k = RMSNorm(sum of
+//                 kv_raw slots) * gamma_ckv, RoPE on k[512:], rounded to bf16
+//                 and written (bf16 or INT8) into the cache row by the fifth
 //   gemm_kernel   q_raw = c^Q @ wq_b, fp32 slots
 //   q_heads_kernel  per (t, h) RMSNorm over 192 of the summed slots, q[:128]
 //                 -> bf16 operand, RoPE(q[128:]) -> q_rope
@@ -25,8 +25,8 @@
 // MN-major: the weights' own row-major layout), the tokens are N (up to 256
 // per work unit), the accumulators double-buffer in TMEM so one unit's
 // epilogue overlaps the next unit's loads.  The norms are memory-bound row
-// passes in fp32 with one rounding to bf16 at each storage point: a
-// 128-thread block per c^Q row, a warp per key row and per (token, head);
+// passes in fp32 with one rounding to bf16 at each storage point: four warps
+// per c^Q row, a warp per key row and per (token, head);
 // they sum the k-split slots in a fixed order, so the result does not depend
 // on scheduling.
 #include <cuda.h>
@@ -115,43 +115,15 @@ __device__ __forceinline__ uint32_t code8(float x, float scale) {
   return static_cast<uint32_t>(static_cast<uint8_t>(static_cast<int8_t>(max(-128, min(127, q)))));
 }
 
-// In place: slot 0 of a partial-sum buffer [slots][n] becomes the sum of all
-// slots, added in slot order (two buffers per launch; n a multiple of 4).
-struct SlotSum {
-  float* buf[2];
-  int64_t n4[2];
-  int slots;
-};
-__global__ void __launch_bounds__(256) sum_slots_kernel(const SlotSum p) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int64_t total = p.n4[0] + p.n4[1];
-  for (int64_t i = blockIdx.x * 256ll + threadIdx.x; i < total; i += static_cast<int64_t>(gridDim.x) * 256) {
-    const int which = i < p.n4[0] ? 0 : 1;
-    const int64_t k = which ? i - p.n4[0] : i;
-    float4* b = reinterpret_cast<float4*>(p.buf[which]) + k;
-    const int64_t stride = p.n4[which];
-    float4 v = b[0];
-#pragma unroll 8
-    for (int sl = 1; sl < p.slots; ++sl) {
-      const float4 w = b[sl * stride];
-      v.x += w.x;
-      v.y += w.y;
-      v.z += w.z;
-      v.w += w.w;
-    }
-    b[0] = v;
-  }
-}
+constexpr int kCqThreads = 128;  // warps 0-3 of a row block: the c^Q row
+constexpr int kRowThreads = kCqThreads + 32;  // warp 4: the key row
+constexpr int kStageCqMax = 12288;  // c^Q rows up to this width are summed once into shared memory
 
-constexpr int kCqThreads = 128;
-
-// One block per c^Q row: sum of squares over the row, then the scaled, rounded row.
-__global__ void __launch_bounds__(kCqThreads) cq_rows_kernel(const NormParams p) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+// The c^Q row of token t by threads 0..127: sum of squares over the row (the
+// slots summed in slot order, staged in shared memory when `stage` is given),
+// then the scaled, rounded row.
+__device__ __forceinline__ void cq_row(const NormParams& p, int t, int tid, float* stage) {
   __shared__ float part[kCqThreads / 32];
-  const int t = blockIdx.x;
   const float4* src = reinterpret_cast<const float4*>(p.c_raw + static_cast<int64_t>(t) * p.q_lora);
   const int64_t slot4 = static_cast<int64_t>(p.T) * p.q_lora / 4;  // one k-split slot, in float4
   const int n4 = p.q_lora >> 2;
@@ -167,35 +139,33 @@ __global__ void __launch_bounds__(kCqThreads) cq_rows_kernel(const NormParams p)
     }
     return v;
   };
+  float4* st4 = reinterpret_cast<float4*>(stage);
   float ss = 0.f;
-  for (int i = threadIdx.x; i < n4; i += kCqThreads) {
+  for (int i = tid; i < n4; i += kCqThreads) {
     const float4 v = row4(i);
+    if (stage != nullptr) st4[i] = v;  // read back below by this same thread
     ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
   }
   ss = warp_sum(ss);
-  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
-  __syncthreads();
+  if ((tid & 31) == 0) part[tid >> 5] = ss;
+  asm volatile("bar.sync 1, %0;" :: "n"(kCqThreads) : "memory");  // warps 0-3 only
   float tot = 0.f;
 #pragma unroll
   for (int w = 0; w < kCqThreads / 32; ++w) tot += part[w];
   const float inv = inv_rms(tot, p.q_lora, p.eps);
   const uint2* gam = reinterpret_cast<const uint2*>(p.gamma_cq);
   uint2* dst = reinterpret_cast<uint2*>(p.c_q + static_cast<int64_t>(t) * p.q_lora);
-  for (int i = threadIdx.x; i < n4; i += kCqThreads) {
-    const float4 v = row4(i);
+  for (int i = tid; i < n4; i += kCqThreads) {
+    const float4 v = stage != nullptr ? st4[i] : row4(i);
     const uint2 gw = __ldg(gam + i);
     dst[i] = make_uint2(pack_bf16(v.x * inv * bf16_lo(gw.x), v.y * inv * bf16_hi(gw.x)),
                         pack_bf16(v.z * inv * bf16_lo(gw.y), v.w * inv * bf16_hi(gw.y)));
   }
 }
 
-// One warp per key row: RMSNorm over the 576-wide row, RoPE on its tail, the cache write.
-__global__ void __launch_bounds__(kWarps * 32) kv_rows_kernel(const NormParams p) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kWarps + warp;
-  if (t >= p.T) return;
+// The key row of token t by one warp: RMSNorm over the 576-wide row, RoPE on
+// its tail, the cache write.
+__device__ __forceinline__ void kv_row(const NormParams& p, int t, int lane) {
   // lane l: latent dims [16 l, 16 l + 16) (eight lanes per 128-element group) and rope pair l
   const float* row = p.kv_raw + static_cast<int64_t>(t) * kKv;
   const int64_t slot = static_cast<int64_t>(p.T) * kKv;  // one k-split slot
@@ -265,6 +235,18 @@ __global__ void __launch_bounds__(kWarps * 32) kv_rows_kernel(const NormParams p
            (code8(xb[4 * k + 3], scale) << 24);
   reinterpret_cast<uint4*>(p.kv_nope + r * kLatent)[lane] = make_uint4(q[0], q[1], q[2], q[3]);
   if ((lane & 7) == 0) p.kv_scales[r * 4 + (lane >> 3)] = scale;
+}
+
+// One block per token: warps 0-3 the c^Q row, warp 4 the key row.
+__global__ void __launch_bounds__(kRowThreads) x_rows_kernel(const NormParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  extern __shared__ float4 stage_c[];
+  const int t = blockIdx.x;
+  if (threadIdx.x < kCqThreads)
+    cq_row(p, t, threadIdx.x, p.q_lora <= kStageCqMax ? reinterpret_cast<float*>(stage_c) : nullptr);
+  else
+    kv_row(p, t, threadIdx.x & 31);
 }
 
 // One warp per (token, head): lane l holds dims (2l, 2l+1), (64+2l, 65+2l) and rope pair l.
@@ -800,21 +782,10 @@ mla_status mla_prolog(const mla_prolog_dims* dims, const void* x, const mla_prol
   gx.job[1] = job_of(T, kKv, hidden, L.sp.x, 1, 0, 0, kv_raw, nullptr, 0);
   ms = launch_gemm(m_wqa, m_x, m_wkv, m_x, gx, sms, s, "x projections launch");
   if (ms != MLA_OK) return ms;
-  if (L.sp.x > 1) {
-    SlotSum ss;
-    ss.buf[0] = c_raw;
-    ss.buf[1] = kv_raw;
-    ss.n4[0] = static_cast<int64_t>(T) * q_lora / 4;
-    ss.n4[1] = static_cast<int64_t>(T) * kKv / 4;
-    ss.slots = L.sp.x;
-    const int64_t blocks = std::min<int64_t>((ss.n4[0] + ss.n4[1] + 255) / 256, static_cast<int64_t>(sms) * 8);
-    PRO_CUDA(launch_chained(sum_slots_kernel, static_cast<unsigned>(blocks), 256, 0, s, ss), "sum_slots_kernel launch");
-  }
-  np.c_slots = 1;
-  np.kv_slots = 1;
-  PRO_CUDA(launch_chained(kv_rows_kernel, static_cast<unsigned>((T + kWarps - 1) / kWarps), kWarps * 32, 0, s, np),
-           "kv_rows_kernel launch");
-  PRO_CUDA(launch_chained(cq_rows_kernel, static_cast<unsigned>(T), kCqThreads, 0, s, np), "cq_rows_kernel launch");
+  np.c_slots = L.sp.x;
+  np.kv_slots = L.sp.x;
+  const size_t row_smem = q_lora <= kStageCqMax ? static_cast<size_t>(q_lora) * 4 : 0;
+  PRO_CUDA(launch_chained(x_rows_kernel, static_cast<unsigned>(T), kRowThreads, row_smem, s, np), "x_rows_kernel launch");
   // c^Q @ wq_b
   GemmParams gb;
   gb.njobs = 1;

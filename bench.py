@@ -22,7 +22,11 @@ Prints one JSON line (rank 0).  ``value`` is microseconds per call (the
 device-timed kernel, CUDA events on the launching stream, L2 flushed by a
 256 MiB write between timed calls); ``e2e`` is the same call made through the
 C ABI with the step's inputs copied from pinned host memory and the outputs
-copied back inside the timed region.  Under torchrun every rank runs its own
+copied back inside the timed region.  For the attention workloads it is
+measured two ways, in order on one stream per step and as a pipelined serving
+loop (copies on their own streams, double-buffered, overlapping the
+neighbouring steps' calls, the L2 flush inside every step); ``e2e.value`` is
+the lower, ``e2e.mode`` names it and both figures are printed.  Under torchrun every rank runs its own
 batch (weak scaling, no collective on the data path); the reported time is
 the maximum over ranks.
 """
@@ -208,6 +212,59 @@ SEEDS = {"tiny_decode": 0, "mtp_decode": 1, "int8_decode": 2, "varlen_decode": 3
 def rank_seed(workload: str, rank: int) -> int:
     """Every rank draws its own batch (weak scaling): the workload's seed plus 1000 per rank."""
     return SEEDS[workload] + 1000 * rank
+
+
+def pipelined_e2e(stream, flush, launch, dev, host_in, steps):
+    """Microseconds per step of a serving loop through the public API: step i's
+    inputs are copied from pinned host memory on an H2D stream, its call runs
+    on `stream` (after the 256 MiB L2 flush, which stays inside the step), and
+    its out/lse are read back to pinned host memory on a D2H stream.  Inputs
+    and outputs are double-buffered, so step i's copies overlap the calls of
+    steps i - 1 and i + 1; every step still copies its own inputs in and its
+    own result out.  Total time from the first H2D to the last read-back,
+    divided by the steps."""
+    import torch
+    names = list(host_in) + ["out", "lse"]
+    bufs = [dict(dev), dict(dev)]
+    for k in names:
+        bufs[1][k] = torch.empty_like(dev[k])
+    host_out = [(dev["out"].cpu().pin_memory(), dev["lse"].cpu().pin_memory()) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_call = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def step(i):
+        j = i % 2
+        b = bufs[j]
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(ev_call[j])  # the call of step i - 2 has read this input buffer
+            for name, t in host_in.items():
+                b[name].copy_(t, non_blocking=True)
+            ev_in[j].record(s_in)
+        stream.wait_event(ev_in[j])
+        stream.wait_event(ev_out[j])  # step i - 2's result has left this output buffer
+        flush.fill_(float(i))
+        launch(b)
+        ev_call[j].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_call[j])
+            host_out[j][0].copy_(b["out"], non_blocking=True)
+            host_out[j][1].copy_(b["lse"], non_blocking=True)
+            ev_out[j].record(s_out)
+
+    for i in range(2):
+        step(i)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    s_in.wait_event(t0)
+    for i in range(steps):
+        step(i)
+    stream.wait_stream(s_out)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) * 1000.0 / steps
 
 
 def reduce_max_over_ranks(values, device):
@@ -434,21 +491,22 @@ def main():
                    cmp_rope=_bf(inp["cmp_rope"]), cmp_scales=_raw(inp.get("cmp_scales")),
                    cmp_block_table=_raw(inp["cmp_block_table"]), cmp_idx=_raw(inp.get("cmp_idx")))
 
-    def launch():
+    def launch(b=None):
+        b = dev if b is None else b
         if cd is not None:
-            mla.mla_compressed_attn_fwd(dev["q_nope"], dev["q_rope"], dev["kv_nope"], dev["kv_rope"],
-                                        dev["kv_scales"], dev["block_table"], dev["cmp_nope"], dev["cmp_rope"],
-                                        dev["cmp_scales"], dev["cmp_block_table"], dev["act_seqs"], dev["out"],
-                                        dev["lse"], window=cd["window"], cmp_ratio=cd["cmp_ratio"],
-                                        cmp_idx=dev["cmp_idx"], softmax_scale=inp["softmax_scale"], mode=mode,
+            mla.mla_compressed_attn_fwd(b["q_nope"], b["q_rope"], b["kv_nope"], b["kv_rope"],
+                                        b["kv_scales"], b["block_table"], b["cmp_nope"], b["cmp_rope"],
+                                        b["cmp_scales"], b["cmp_block_table"], b["act_seqs"], b["out"],
+                                        b["lse"], window=cd["window"], cmp_ratio=cd["cmp_ratio"],
+                                        cmp_idx=b["cmp_idx"], softmax_scale=inp["softmax_scale"], mode=mode,
                                         dims=dims, stream=stream)
         elif window:
-            mla.mla_swa_fwd(dev["q_nope"], dev["q_rope"], dev["kv_nope"], dev["kv_rope"], dev["kv_scales"],
-                            dev["block_table"], dev["act_seqs"], dev["out"], dev["lse"], window=window,
+            mla.mla_swa_fwd(b["q_nope"], b["q_rope"], b["kv_nope"], b["kv_rope"], b["kv_scales"],
+                            b["block_table"], b["act_seqs"], b["out"], b["lse"], window=window,
                             softmax_scale=inp["softmax_scale"], mode=mode, dims=dims, stream=stream)
         else:
-            mla.mla_sparse_attn_fwd(dev["q_nope"], dev["q_rope"], dev["kv_nope"], dev["kv_rope"], dev["kv_scales"],
-                                    dev["topk_idx"], dev["block_table"], dev["act_seqs"], dev["out"], dev["lse"],
+            mla.mla_sparse_attn_fwd(b["q_nope"], b["q_rope"], b["kv_nope"], b["kv_rope"], b["kv_scales"],
+                                    b["topk_idx"], b["block_table"], b["act_seqs"], b["out"], b["lse"],
                                     softmax_scale=inp["softmax_scale"], mode=mode, dims=dims, stream=stream)
 
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
@@ -521,13 +579,15 @@ def main():
             e_e[k].record(stream)
     torch.cuda.synchronize()
     e2e_ms = [s.elapsed_time(e) for s, e in zip(e_s, e_e)]
+    pipe_us = pipelined_e2e(stream, flush, launch, dev, host_in, e2e_steps)
     clock_summary = clocks.stop()
 
     # median of the cold-L2 calls (the headline); mean and the warm back-to-back figure beside it
     us = float(np.median(times_ms) * 1000.0)
     mean_us = float(np.mean(times_ms) * 1000.0)
     e2e_us = float(np.median(e2e_ms) * 1000.0)
-    us, e2e_us, mean_us, warm_us = reduce_max_over_ranks([us, e2e_us, mean_us, warm_us], device="cuda")
+    us, e2e_us, mean_us, warm_us, pipe_us = reduce_max_over_ranks([us, e2e_us, mean_us, warm_us, pipe_us],
+                                                                  device="cuda")
 
     if rank == 0:
         hbm_gbs, bf16_tf, peak_src = measured_peaks()
@@ -558,8 +618,17 @@ def main():
             "roofline": roofline_of(counts, us, hbm_gbs, bf16_tf, peak_src, traffic),
             "tensor": {"achieved_tflops": round(tflops, 2), "peak_tflops": bf16_tf,
                        "frac": round(tflops / bf16_tf, 4), "flops_per_launch": counts["flops"]},
-            "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-                    "d2h_bytes_per_step": int(d2h)},
+            "e2e": {"value": round(min(pipe_us, e2e_us), 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": int(d2h),
+                    "mode": "pipelined" if pipe_us <= e2e_us else "serial",
+                    "pipelined_us": round(pipe_us, 3),
+                    "pipelined_mode": "serving loop: each step copies its inputs in (H2D stream) and its out/lse "
+                                      "back (D2H stream), double-buffered so copies overlap the neighbouring "
+                                      "steps' calls; the L2 flush stays inside each step; total time / steps",
+                    "serial_us": round(e2e_us, 3),
+                    "serial_mode": "copies, call and read-back in order on one stream, L2 flushed before each "
+                                   "step outside its events; median per step",
+                    "value_is": "the lower of the two"},
             "gpu_launches": launches,
             "clocks": clock_summary,
             "device_status": status,

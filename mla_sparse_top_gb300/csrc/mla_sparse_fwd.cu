@@ -18,13 +18,15 @@
 // Per CTA (24 warps; registers rebalanced per warpgroup with setmaxnreg):
 //   warps 0-7   softmax: TMEM lane h = head h; warps w and w+4 share the
 //               lanes of quadrant w % 4 and take key columns [32c, 32c+32),
-//               c = w / 4.  Load Q (latent dims [0, 128) into TMEM, [128, 256)
-//               and the rope dims into smem); per tile read the own partial S,
+//               c = w / 4.  Per tile read the own partial S,
 //               add the peer's, mask and scale, row max across the warp pair,
 //               lazy online softmax, write P over S in its TMEM region as
 //               P_hi = bf16(p), P_lo = bf16(p - P_hi); final O / l -> bf16, lse.
 //   warps 8-11  senders: partial S tile -> staging buffer -> bulk copies to
-//               the peer, one 32-key column half at a time.
+//               the peer, one 32-key column half at a time; each token's Q
+//               (latent dims [0, 128) into TMEM, [128, 256) and the rope dims
+//               into smem) as soon as the previous token's score MMAs are
+//               complete (INT8 instantiations: the softmax warps load Q).
 //   warps 12-19 gather: all eight warps on every key tile (8 keys each); bf16
 //               cache by cp.async with zero fill for masked entries, INT8
 //               cache by loads, dequantisation to bf16 and stores.
@@ -560,14 +562,63 @@ __device__ __forceinline__ bool send_half(const Ctx& c, const uint32_t (&v)[32],
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
+// Q of token qrow / n_q, one sender thread per head h: the CTA's latent dims
+// [128, 256) (128-byte swizzled rows of 64 dims, head h at row h of chunk
+// (d - 128) / 64) and its 32 rope dims go to shared memory by cp.async
+// (zero-filled for heads beyond n_q), then dims [0, 128) to TMEM (the lanes
+// of the thread's quadrant) through registers; then QReady.  The senders load
+// each token's Q as soon as the previous token's score MMAs are complete, so
+// the load overlaps the softmax of that token's last tiles.
+__device__ __forceinline__ void load_q(const Params& p, const Ctx& c, int h, bool live, int64_t qrow, uint32_t tQ) {
+  const uint8_t* qn = reinterpret_cast<const uint8_t*>(p.q_nope) + (qrow * 512 + c.crank * 256) * 2;
+  const uint8_t* qr = reinterpret_cast<const uint8_t*>(p.q_rope) + (qrow * 64 + c.crank * 32) * 2;
+  const uint32_t nb = live ? 16u : 0u;
+#pragma unroll
+  for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      cp_async_16(c.sbase + kOffQHalf + ch * (kQHalfBytes / 2) + h * 128 + ((u ^ (h & 7)) << 4),
+                  live ? static_cast<const void*>(qn + 256 + (8 * ch + u) * 16) : p.q_nope, nb);
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    cp_async_16(c.sbase + kOffQRope + rope_unit(h, u), live ? static_cast<const void*>(qr + u * 16) : p.q_rope, nb);
+  // all register loads are issued before the first TMEM store
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  uint4 qv[16];
+#pragma unroll
+  for (int u = 0; u < 16; ++u) qv[u] = live ? ldg16(qn + u * 16) : zero;
+#pragma unroll
+  for (int ch = 0; ch < 2; ++ch) {
+    uint32_t w[32];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      w[4 * u + 0] = qv[8 * ch + u].x;
+      w[4 * u + 1] = qv[8 * ch + u].y;
+      w[4 * u + 2] = qv[8 * ch + u].z;
+      w[4 * u + 3] = qv[8 * ch + u].w;
+    }
+    tmem_st_32x32b_x32(tQ + 32 * ch, w);
+  }
+  cp_async_wait_all();
+  fence_proxy_async_smem();  // cp.async data -> tensor-core reads
+  tmem_wait_st();
+  tc_fence_before();
+  mbar_arrive(c.bar(kBarQReady));
+}
+
+template <bool kInt8, int kMode>
 __device__ void sender_role(const Params& p, const Ctx& c, int q, int lane) {
   const int h = q * 32 + lane;
+  const bool live = h < p.n_q;
+  const uint32_t tQ = c.tmem + (static_cast<uint32_t>(q * 32) << 16) + kTmemQ;
   const uint32_t tR = c.tmem + (static_cast<uint32_t>(q * 32) << 16) + kTmemRegion;
   const uint32_t peer = c.crank ^ 1u;
   const uint32_t stg = c.sbase + kOffStaging;
   const uint32_t dst = mapa_shared(c.sbase + kOffRecv, peer);
   const uint32_t rbar0 = mapa_shared(c.bar(kBarRecvFull + 0), peer);
   const uint32_t rbar1 = mapa_shared(c.bar(kBarRecvFull + 1), peer);
+  if constexpr (!kInt8) load_q(p, c, h, live, static_cast<int64_t>(token_of<kMode>(p, c, 0)) * p.n_q + h, tQ);
+  int m = 0, m_end = seg_end<kMode>(p, c, 0);  // token ordinal and the end of its segment
   // the loop bound comes from shared memory: the two 32-column halves held in
   // registers leave none to spare for it
   for (int j = 0; j < lds_s32(c.sbase + kOffTotal); ++j) {
@@ -582,6 +633,14 @@ __device__ void sender_role(const Params& p, const Ctx& c, int q, int lane) {
     mbar_arrive_relaxed(c.bar(kBarSFree + r));  // the values are in registers (wait::ld)
     if (!send_half(c, a, h, q, lane, j, 0, stg, dst, rbar0)) break;
     if (!send_half(c, b, h, q, lane, j, 1, stg + kXchgBytes, dst + kXchgBytes, rbar1)) break;
+    if (!kInt8 && j + 1 == m_end && m + 1 < c.ntok) {
+      // the next token's Q replaces this one's once its score MMAs are complete
+      if (!warp_wait(c, kBarQFree, m & 1)) break;
+      tc_fence_after();
+      ++m;
+      load_q(p, c, h, live, static_cast<int64_t>(token_of<kMode>(p, c, m)) * p.n_q + h, tQ);
+      m_end = seg_end<kMode>(p, c, m);
+    }
   }
   // the peer cannot leave before this CTA reaches its final cluster barrier,
   // which waits for these copies to complete
@@ -694,12 +753,14 @@ __device__ void mma_role(const Params& p, const Ctx& c) {
 }
 
 // ------------------------------------------------------------------ softmax warps
+// INT8 instantiations: Q loaded by the softmax warps themselves (two threads
+// per head), measured faster there than the sender-side load above.
 // Q of token qrow / n_q: latent dims [128 half, 128 half + 128) of the CTA's
 // 256 (the lower half to TMEM, the upper half to shared memory as 128-byte
 // swizzled rows of 64 dims, head h at row h of chunk (d - 128) / 64) and the
 // CTA's rope dims; then QReady.
-__device__ __forceinline__ void load_q(const Params& p, const Ctx& c, int h, int half, bool live, int64_t qrow,
-                                       uint32_t tQ) {
+__device__ __forceinline__ void load_q_softmax(const Params& p, const Ctx& c, int h, int half, bool live,
+                                               int64_t qrow, uint32_t tQ) {
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
   {
     // All loads are issued before the first store: a shared-memory or TMEM store
@@ -850,7 +911,7 @@ __global__ void __launch_bounds__(kHeads) combine_kernel(const __grid_constant__
 // Q of token m + 1 (once QFree says the score MMAs of token m are complete),
 // so the next token's first score tiles are computed while O of token m is
 // read out; after reading O they arrive on OFree.
-template <int kMode>
+template <bool kInt8, int kMode>
 __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) {
   const int q = warp & 3;          // TMEM lane quadrant
   const int half = warp >> 2;      // key columns [32 half, 32 half + 32)
@@ -858,9 +919,10 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
   const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
   const uint32_t tR = c.tmem + lane_off + kTmemRegion;  // + 64 * (i % kRegions)
   const uint32_t tO = c.tmem + lane_off + kTmemO + 128 * half;
-  const uint32_t tQ = c.tmem + lane_off + kTmemQ;
   const bool live = h < p.n_q;
-  load_q(p, c, h, half, live, static_cast<int64_t>(token_of<kMode>(p, c, 0)) * p.n_q + h, tQ);
+  if constexpr (kInt8)
+    load_q_softmax(p, c, h, half, live, static_cast<int64_t>(token_of<kMode>(p, c, 0)) * p.n_q + h,
+                   c.tmem + lane_off + kTmemQ);
   const uint32_t peer = c.crank ^ 1u;
   const uint32_t dep_zero = *reinterpret_cast<volatile uint32_t*>(c.smem + kOffZero);
   float* pair = reinterpret_cast<float*>(c.smem + kOffPair);
@@ -984,11 +1046,14 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
 
     }
     if (!ok) return;
-    if (mt + 1 < c.ntok) {
-      // the next token's Q replaces this one's once its score MMAs are complete
-      if (!warp_wait(c, kBarQFree, mt & 1)) return;
-      tc_fence_after();
-      load_q(p, c, h, half, live, static_cast<int64_t>(token_of<kMode>(p, c, mt + 1)) * p.n_q + h, tQ);
+    if constexpr (kInt8) {
+      if (mt + 1 < c.ntok) {
+        // the next token's Q replaces this one's once its score MMAs are complete
+        if (!warp_wait(c, kBarQFree, mt & 1)) return;
+        tc_fence_after();
+        load_q_softmax(p, c, h, half, live, static_cast<int64_t>(token_of<kMode>(p, c, mt + 1)) * p.n_q + h,
+                       c.tmem + lane_off + kTmemQ);
+      }
     }
     // l over the whole row: add the partner's column half (same order in both threads)
     float* slot_l = pair + (pa & 1) * 2 * kHeads;
@@ -1083,7 +1148,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_spa
       mbar_init(c.bar(kBarPeerFree + h2), kSoftmaxThreads / 2);  // the four warps reading that column half
     }
     for (int q = 0; q < 4; ++q) mbar_init(c.bar(kBarPairA + q), 64);
-    mbar_init(c.bar(kBarQReady), kSoftmaxThreads);
+    mbar_init(c.bar(kBarQReady), kInt8 ? kSoftmaxThreads : kSenderThreads);
     mbar_init(c.bar(kBarQFree), 1);
     mbar_init(c.bar(kBarOFree), kSoftmaxThreads);
     mbar_init(c.bar(kBarFinal), 1);
@@ -1108,9 +1173,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_spa
 
   if (warp < kSenderWarp0) {
     regs_increase<Regs<kInt8>::kSoftmax>();
-    if (!*c.abort) softmax_role<kMode>(p, c, warp, lane);
+    if (!*c.abort) softmax_role<kInt8, kMode>(p, c, warp, lane);
   } else if (warp < kGatherWarp0) {
-    if (!*c.abort) sender_role(p, c, warp - kSenderWarp0, lane);
+    if (!*c.abort) sender_role<kInt8, kMode>(p, c, warp - kSenderWarp0, lane);
   } else if (warp < kMmaWarp) {
     regs_decrease<Regs<kInt8>::kGather>();
     if (!*c.abort) gather_role<kInt8, kMode>(p, c, warp - kGatherWarp0, lane);

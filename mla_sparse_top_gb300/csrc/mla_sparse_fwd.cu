@@ -393,6 +393,10 @@ __device__ void index_role(const Params& p, const Ctx& c, int iw, int lane, int 
                      : -1;
       }
     }
+    // the sequence lengths too, so that their latency overlaps the table loads
+    int act[kIdxBatch];
+#pragma unroll
+    for (int k = 0; k < kIdxBatch; ++k) act[k] = k < nb ? __ldg(p.act_seqs + seq_of_tile<kMode>(p, c, j0 + k)) : 0;
     int nxt[8];
     index_load<kMode>(p, c, j0 + kIndexWarps * kIdxBatch, lane, nxt);
     bool ok = true;
@@ -404,13 +408,12 @@ __device__ void index_role(const Params& p, const Ctx& c, int iw, int lane, int 
 #pragma unroll
     for (int k = 0; k < kIdxBatch; ++k) {
       if (k >= nb) continue;
-      const int act = __ldg(p.act_seqs + seq_of_tile<kMode>(p, c, j0 + k));
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int q = 2 * k + u;
         // a compressed entry was checked for visibility when it was loaded
         const bool cmp = kMode == kModeCompressed && idx[q] >= 0 && (idx[q] & kCmpFlag);
-        const bool in_seq = idx[q] >= 0 && (cmp || idx[q] < act);
+        const bool in_seq = idx[q] >= 0 && (cmp || idx[q] < act[k]);
         const bool valid = in_seq && blk[q] >= 0 && blk[q] < (cmp ? p.cmp_num_blocks : p.num_blocks);
         if (in_seq && !valid) bad = true;
         const int row = (blk[q] * 128 + (idx[q] & 127)) | (cmp ? kCmpFlag : 0);
@@ -1075,13 +1078,14 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
     const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
     uint4* op = reinterpret_cast<uint4*>(p.out + qrow * 512 + c.crank * 256 + half * 128);
 #pragma unroll 1
-    for (int ch = 0; ch < 4; ++ch) {
-      uint32_t o[32];
-      tmem_ld_32x32b_x32(tO + 32 * ch, o);
+    for (int ch = 0; ch < 4; ch += 2) {
+      uint32_t o[64];  // two 32-column chunks per TMEM wait
+      tmem_ld_32x32b_x32(tO + 32 * ch, *reinterpret_cast<uint32_t(*)[32]>(o));
+      tmem_ld_32x32b_x32(tO + 32 * ch + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
       tmem_wait_ld();
       if (live) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < 8; ++k) {
           uint4 w;
           w.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l);
           w.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l);

@@ -298,12 +298,14 @@ idx_scores_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
 }
 
 // ------------------------------------------------------------------ selection
-constexpr int kSelThreads = 512;
+constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kRegChunks = 16;                       // scores of the first 8192 positions live in registers
+constexpr int kRegChunks = 8;                        // scores of the first 8192 positions live in registers
 constexpr int kSelGroup = kRegChunks * kSelThreads;  // positions per segment
 constexpr int kBuckets = 2048;                       // value buckets of the first selection step
 constexpr int kListCap = 256;                        // threshold-bucket keys ranked directly
+constexpr int kBucketsPerThread = kBuckets / kSelThreads;  // the bucket scan's share of each thread
+static_assert(kBucketsPerThread * kSelThreads == kBuckets && kRegChunks * kSelWarps == 256, "selection layout");
 
 struct SelectParams {
   const float* scores;
@@ -337,7 +339,7 @@ __device__ __forceinline__ int value_bucket(float v, float lo_half, float scale)
   return static_cast<int>(fminf(x, static_cast<float>(kBuckets - 1)));
 }
 
-// One CTA per token.  Position j = g * 8192 + c * 512 + tid sits in chunk c of
+// One CTA per token.  Position j = g * 8192 + c * 1024 + tid sits in chunk c of
 // segment g; segment 0 keeps its scores in registers, later segments (sequences
 // longer than 8192) reload theirs.  The selection keeps every key above a
 // threshold key T and the first k_rem keys equal to T, in position order:
@@ -442,11 +444,11 @@ __global__ void __launch_bounds__(kSelThreads) idx_topk_kernel(const SelectParam
         }
       }
       __syncthreads();
-      // thread i holds buckets 2047-4i .. 2044-4i (descending); block scan in thread order
-      uint32_t h4[4], s4 = 0;
+      // thread i holds buckets 2047 - kBucketsPerThread i downwards; block scan in thread order
+      uint32_t h4[kBucketsPerThread], s4 = 0;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        h4[e] = hb[kBuckets - 1 - 4 * tid - e];
+      for (int e = 0; e < kBucketsPerThread; ++e) {
+        h4[e] = hb[kBuckets - 1 - kBucketsPerThread * tid - e];
         s4 += h4[e];
       }
       uint32_t incl = s4;
@@ -463,10 +465,10 @@ __global__ void __launch_bounds__(kSelThreads) idx_topk_kernel(const SelectParam
       const uint32_t excl = incl - s4;
       if (incl >= topk && excl < topk) {
         uint32_t cum = excl, mb = 0;
-        int eb = 3;
+        int eb = kBucketsPerThread - 1;
         bool found = false;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int e = 0; e < kBucketsPerThread; ++e) {
           if (!found) {
             if (cum + h4[e] >= topk) {
               found = true;
@@ -477,7 +479,7 @@ __global__ void __launch_bounds__(kSelThreads) idx_topk_kernel(const SelectParam
             }
           }
         }
-        bcast[0] = static_cast<uint32_t>(kBuckets - 1 - 4 * tid - eb);
+        bcast[0] = static_cast<uint32_t>(kBuckets - 1 - kBucketsPerThread * tid - eb);
         bcast[1] = cum;
         bcast[2] = mb;
       }
@@ -564,7 +566,7 @@ __global__ void __launch_bounds__(kSelThreads) idx_topk_kernel(const SelectParam
           }
         }
         // the other histogram is free: clear it for the next pass
-        if (tid >= 256) hb[((pass + 1) & 1) * 256 + tid - 256] = 0;
+        if (tid >= 256 && tid < 512) hb[((pass + 1) & 1) * 256 + tid - 256] = 0;
         __syncthreads();
         prefix |= bcast[6] << shift;
         k_left -= bcast[7];

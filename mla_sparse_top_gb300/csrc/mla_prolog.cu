@@ -414,6 +414,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap w0, const __grid_constant__ CUte
     // MMA issue
     if (lane == 0) {
       constexpr uint32_t idesc = make_idesc_f16(128, 128, 1, 1, 0);
+      constexpr uint32_t idesc256 = make_idesc_f16(128, 256, 1, 1, 0);
       int it = 0, lu = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x, ++lu) {
@@ -430,6 +431,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap w0, const __grid_constant__ CUte
           if (!ok) break;
           tc_fence_after();
           const uint32_t stage = sb + st * kGemmStageBytes;
+          if (fsub == 1 && nt == 2) {
+            // both 128-token halves in one N = 256 MMA: their boxes are contiguous
+            // in the stage and their accumulator blocks (0, 0) and (0, 1) in TMEM
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              umma_ss(d, make_sdesc(stage + kOffW + ks * 16 * 128, kBoxBytes, 1024, kSwizzle128B),
+                      make_sdesc(stage + kOffX + ks * 32, 16, 1024, kSwizzle128B), idesc256,
+                      (kb > g.k0 || ks > 0) ? 1u : 0u);
+            umma_commit(bar(kEmpty + st));
+            continue;
+          }
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
             const uint32_t acc = (kb > g.k0 || ks > 0) ? 1u : 0u;

@@ -484,22 +484,31 @@ gemm_kernel(const __grid_constant__ CUtensorMap w0, const __grid_constant__ CUte
             const int tb = g.tt * 128 * tsub + 128 * h;
             if (tb >= p.T) break;
 #pragma unroll 1
-            for (int ch = 0; ch < 4; ++ch) {
-              uint32_t v[32];
-              tmem_ld_32x32b_x32(tmem + lanes + 256 * a + 128 * (fs + h) + 32 * ch, v);
+            for (int ch = 0; ch < 4; ch += 2) {
+              uint32_t v[64];  // two 32-token chunks per TMEM wait
+              tmem_ld_32x32b_x32(tmem + lanes + 256 * a + 128 * (fs + h) + 32 * ch,
+                                 *reinterpret_cast<uint32_t(*)[32]>(v));
+              tmem_ld_32x32b_x32(tmem + lanes + 256 * a + 128 * (fs + h) + 32 * ch + 32,
+                                 *reinterpret_cast<uint32_t(*)[32]>(v + 32));
               tmem_wait_ld();
               const int t0 = tb + 32 * ch;
-              if (fin) {
+              const int nv = p.T - t0;  // tokens of these chunks inside the call (>= 64: all)
+              if (fin && nv > 0) {
                 if (J.out_f32 != nullptr) {
                   float* o = J.out_f32 + (static_cast<int64_t>(g.s) * p.T + t0) * J.F + f;
+                  if (nv >= 64) {
 #pragma unroll
-                  for (int k = 0; k < 32; ++k)
-                    if (t0 + k < p.T) o[static_cast<int64_t>(k) * J.F] = __uint_as_float(v[k]);
+                    for (int k = 0; k < 64; ++k) o[static_cast<int64_t>(k) * J.F] = __uint_as_float(v[k]);
+                  } else {
+#pragma unroll
+                    for (int k = 0; k < 64; ++k)
+                      if (k < nv) o[static_cast<int64_t>(k) * J.F] = __uint_as_float(v[k]);
+                  }
                 } else {
                   uint16_t* o = J.out_bf16 + static_cast<int64_t>(t0) * J.out_ld + static_cast<int64_t>(g.b) * J.F + f;
 #pragma unroll
-                  for (int k = 0; k < 32; ++k)
-                    if (t0 + k < p.T) {
+                  for (int k = 0; k < 64; ++k)
+                    if (nv >= 64 || k < nv) {
                       const __nv_bfloat16 hv = __float2bfloat16_rn(__uint_as_float(v[k]));
                       o[static_cast<int64_t>(k) * J.out_ld] = *reinterpret_cast<const uint16_t*>(&hv);
                     }

@@ -28,7 +28,8 @@
  *     an equal share, a token cut between clusters leaves one partial softmax
  *     state per part in the buffer, and a second launch merges them.  The
  *     buffer (~40 MB on a GB300) is allocated by the first such call on the
- *     stream and kept for the life of the process.  A first such call on a
+ *     stream and kept for the life of the process (mla_sparse_allow_cut_tokens(0)
+ *     turns this off: whole tokens, no buffer).  A first such call on a
  *     stream that is capturing a CUDA graph allocates nothing and schedules
  *     whole tokens instead (same results, less even load).  Calls on one
  *     stream share its buffer in stream order; a captured graph uses the
@@ -227,6 +228,17 @@ mla_status mla_sparse_set_wait_limit_ns(uint64_t ns);
  * and the merge of the cut tokens' parts).  For accounting only.
  */
 uint64_t mla_sparse_launch_count(void);
+
+/*
+ * mla_sparse_allow_cut_tokens -- whether later attention calls may give the
+ * persistent clusters equal shares of the key tiles, cutting tokens between
+ * them (allow != 0, the default), or always schedule whole tokens (0).  With
+ * 0 the library never allocates its buffer for cut tokens and every call is a
+ * single launch; results are the same either way, only the load balance of
+ * calls with few tokens and long lists differs.  Applies to all threads of
+ * the process.
+ */
+void mla_sparse_allow_cut_tokens(int32_t allow);
 
 /* ABI version of this header (major * 100 + minor). */
 int32_t mla_sparse_abi_version(void);

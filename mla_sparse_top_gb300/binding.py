@@ -31,6 +31,7 @@ MLA_DEVICE_TIMEOUT = 0x2
 
 EXPORTED_SYMBOLS = ("mla_sparse_attn_fwd", "mla_swa_fwd", "mla_compressed_attn_fwd", "mla_sparse_last_error", "mla_sparse_device_status",
                     "mla_sparse_get_device_status", "mla_sparse_set_wait_limit_ns", "mla_sparse_launch_count",
+                    "mla_sparse_allow_cut_tokens",
                     "mla_sparse_abi_version", "mla_indexer_workspace_bytes", "mla_indexer_topk",
                     "mla_indexer_scores", "mla_indexer_select", "mla_indexer_device_status",
                     "mla_indexer_last_error", "mla_indexer_topk_noalloc", "mla_cache_write",
@@ -106,6 +107,8 @@ def load_library(path: str = LIB_PATH):
     lib.mla_sparse_set_wait_limit_ns.restype = ctypes.c_int
     lib.mla_sparse_launch_count.argtypes = []
     lib.mla_sparse_launch_count.restype = ctypes.c_uint64
+    lib.mla_sparse_allow_cut_tokens.argtypes = [ctypes.c_int32]
+    lib.mla_sparse_allow_cut_tokens.restype = None
     lib.mla_sparse_abi_version.argtypes = []
     lib.mla_sparse_abi_version.restype = ctypes.c_int32
     lib.mla_indexer_workspace_bytes.argtypes = [ctypes.POINTER(IndexerDims)]
@@ -300,6 +303,11 @@ DEFAULT_WAIT_LIMIT_NS = 500 * 1000 * 1000
 def launch_count() -> int:
     """Kernel launches the attention entry points have enqueued in this process."""
     return int(load_library().mla_sparse_launch_count())
+
+
+def allow_cut_tokens(allow: bool) -> None:
+    """Whether later attention calls may cut tokens between clusters (the default)."""
+    load_library().mla_sparse_allow_cut_tokens(1 if allow else 0)
 
 
 # ------------------------------------------------------------------ Lightning Indexer

@@ -1282,6 +1282,8 @@ constexpr int64_t kMinPartTiles = 2;
 
 // Kernel launches enqueued by the attention entry points.
 std::atomic<unsigned long long> g_launches{0};
+// Whether calls may cut tokens between clusters (and so allocate the buffer).
+std::atomic<int> g_allow_cut{1};
 
 // Bound of every device-side wait of the next launches (nanoseconds).
 std::atomic<unsigned long long> g_wait_ns{500ull * 1000ull * 1000ull};
@@ -1329,7 +1331,7 @@ cudaError_t prepare_kernel(int dev) {
 
 extern "C" {
 
-int32_t mla_sparse_abi_version(void) { return 201; }
+int32_t mla_sparse_abi_version(void) { return 202; }
 
 const char* mla_sparse_last_error(void) { return g_last_error; }
 
@@ -1442,7 +1444,7 @@ mla_status attn_fwd(const mla_dims* dims, const void* q_nope, const void* q_rope
     return fail(MLA_ERR_SHAPE, "B*S1 x key tiles per token = %lld too large", static_cast<long long>(tiles));
   p.ws = nullptr;
   p.n_clusters = static_cast<int>(T < max_clusters ? T : max_clusters);
-  if (kmode == mlasp::kModeLists) {
+  if (kmode == mlasp::kModeLists && g_allow_cut.load(std::memory_order_relaxed)) {
     const int64_t nc_equal = std::min<int64_t>(max_clusters, std::max<int64_t>(1, tiles / kMinPartTiles));
     const int64_t most_whole = (T + p.n_clusters - 1) / p.n_clusters * p.n_tiles;
     const int64_t most_equal = (tiles + nc_equal - 1) / nc_equal;
@@ -1548,6 +1550,8 @@ mla_status mla_sparse_set_wait_limit_ns(uint64_t ns) {
 mla_status mla_sparse_get_device_status(void* stream) { return mla_sparse_device_status(stream, nullptr, 0); }
 
 uint64_t mla_sparse_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+void mla_sparse_allow_cut_tokens(int32_t allow) { g_allow_cut.store(allow ? 1 : 0, std::memory_order_relaxed); }
 
 mla_status mla_sparse_device_status(void* stream, uint32_t* flags, int32_t clear) {
   g_last_error[0] = '\0';

@@ -35,7 +35,7 @@ def test_header_declares_the_entry_points():
             "mla_indexer_select", "mla_indexer_topk_noalloc", "mla_cache_write", "mla_cache_last_error",
             "mla_cache_device_status", "mla_swa_fwd", "mla_compressed_attn_fwd", "mla_prolog",
             "mla_prolog_workspace_bytes", "mla_prolog_last_error", "mla_prolog_device_status",
-            "mla_sparse_get_device_status", "mla_sparse_set_wait_limit_ns", "mla_sparse_launch_count"} <= set(names)
+            "mla_sparse_get_device_status", "mla_sparse_set_wait_limit_ns", "mla_sparse_launch_count", "mla_sparse_allow_cut_tokens"} <= set(names)
 
 
 def test_library_exports_every_declared_function(lib):
@@ -43,7 +43,7 @@ def test_library_exports_every_declared_function(lib):
         assert hasattr(lib, name), name
     from mla_sparse_top_gb300 import binding
     assert set(binding.EXPORTED_SYMBOLS) == set(declared_functions())
-    assert lib.mla_sparse_abi_version() == 201
+    assert lib.mla_sparse_abi_version() == 202
 
 
 @pytest.mark.parametrize("ns, expect", [(0, -2), (999, -2), (60 * 10**9 + 1, -2), (1000, 0), (500 * 10**6, 0)])

@@ -93,3 +93,26 @@ def test_graph_capture_with_and_without_the_buffer():
         assert_out_close(out, ref_out, f"captured with the buffer, replay {rep}")
         assert_lse_close(lse, ref_lse, f"captured with the buffer, replay {rep}")
     assert mla.device_status(clear=True) == 0
+
+
+def test_whole_tokens_when_cutting_is_turned_off():
+    """mla_sparse_allow_cut_tokens(0): one launch per call, no buffer, same results."""
+    import mla_sparse_top_gb300 as mla
+    inp = workloads.make_inputs(B=2, S1=2, n_q=128, act_seqs=[8192, 6000], topk=2048, seed=86)
+    ref_out, ref_lse, _ = oracle.forward(inp)
+    dev = to_device(inp)
+    try:
+        mla.allow_cut_tokens(False)
+        n0 = mla.launch_count()
+        out, lse, status = run_gpu(inp, dev=dev)
+        assert mla.launch_count() - n0 == 1
+    finally:
+        mla.allow_cut_tokens(True)
+    assert status == 0
+    assert_out_close(out, ref_out, "whole tokens")
+    assert_lse_close(lse, ref_lse, "whole tokens")
+    n0 = mla.launch_count()
+    out2, lse2, status2 = run_gpu(inp, dev=dev)
+    assert mla.launch_count() - n0 == 2, "four tokens of 32 tiles should be cut between clusters"
+    assert status2 == 0
+    assert_out_close(out2, ref_out, "cut tokens")

@@ -21,7 +21,9 @@
  *
  * Conventions are those of mla_sparse.h: device pointers owned by the caller,
  * asynchronous on `stream`, argument errors returned before any launch with
- * mla_indexer_last_error() describing them, every internal wait bounded.
+ * mla_indexer_last_error() describing them, every internal wait bounded
+ * (mla_sparse_set_wait_limit_ns); a wait that runs out makes that launch give
+ * up and raises MLA_DEVICE_TIMEOUT, and the next launch runs in full.
  * Numerics: q and k bf16, products exact, dot products and the head sum in
  * fp32 (tensor cores, fp32 accumulate); the selection compares those fp32
  * scores exactly.

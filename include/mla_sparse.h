@@ -210,8 +210,11 @@ mla_status mla_sparse_get_device_status(void* stream);
 
 /*
  * mla_sparse_set_wait_limit_ns -- bound, in nanoseconds, of every device-side
- * wait of the attention launches enqueued after this call (all threads of the
- * process; default 500 ms).  No counterpart in the pages: the pages' runtime
+ * wait of the library's launches enqueued after this call: the attention
+ * kernels, the Lightning Indexer's score kernel and the MLA Prolog's product
+ * kernel (all threads of the process; default 500 ms).  Waits that only let
+ * copies or MMAs already in flight land before a block exits keep at least
+ * 500 ms.  No counterpart in the pages: the pages' runtime
  * debug mode ("DeepSeek V3/V2 Sparse Flash Attention with Quantization",
  * notes) checks the operator while it runs; this bound is what turns a stall
  * into MLA_DEVICE_TIMEOUT instead of a hang.  Accepted range [1 us, 60 s];

@@ -43,6 +43,10 @@
 #include "../../include/mla_indexer.h"
 #include "ptx.cuh"
 
+namespace mlasp {
+unsigned long long host_wait_limit_ns();  // the library's wait bound (mla_sparse_set_wait_limit_ns)
+}
+
 namespace mlaidx {
 using namespace mlasp;
 
@@ -78,7 +82,9 @@ static_assert(kOffAbort + 4 <= kOffQ, "small items fit below Q");
 static_assert(kOffQ % 1024 == 0 && kTileBytes % 1024 == 0, "operand alignment");
 static_assert(kOffQ + 2 * kMaxN * 128 + 2 * kTileBytes <= kSmemMax, "at least two stages at the largest N");
 
-constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;
+// Waits that only let copies or MMAs already in flight land before the CTA
+// exits are never cut shorter than this, whatever the configured bound.
+constexpr uint64_t kDrainWaitNs = 500ull * 1000ull * 1000ull;
 
 __device__ unsigned int g_idx_status = 0;
 
@@ -95,17 +101,19 @@ struct ScoreParams {
   uint32_t q_chunk;     // bytes of one 64-dim chunk of Q: N * 128
   uint32_t off_stages;  // shared-memory offset of the key ring
   uint32_t tmem_cols;
+  unsigned long long wait_ns;  // bound of every wait (mla_sparse_set_wait_limit_ns)
 };
 
 struct Ctx {
   uint32_t sbase;
   uint8_t* smem;
   volatile uint32_t* abort;
+  uint64_t wait_ns;
   __device__ uint32_t bar(int i) const { return sbase + kOffBars + 8 * i; }
 };
 
 __device__ __forceinline__ bool wait_bar(const Ctx& c, int idx, uint32_t parity) {
-  return mbar_wait<false>(c.bar(idx), parity, c.abort, kWaitLimitNs);
+  return mbar_wait<false>(c.bar(idx), parity, c.abort, c.wait_ns);
 }
 __device__ __forceinline__ bool warp_wait(const Ctx& c, int idx, uint32_t parity) {
   return __all_sync(0xffffffffu, wait_bar(c, idx, parity));
@@ -157,9 +165,12 @@ idx_scores_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
   c.smem = smem;
   c.sbase = smem_u32(smem);
   c.abort = reinterpret_cast<volatile uint32_t*>(smem + kOffAbort);
+  c.wait_ns = p.wait_ns;
   if (tid == 0) {
+    // each launch starts afresh: a timeout of an earlier launch stays in the
+    // status word until it is cleared but does not stop this one
     const bool misaligned = (c.sbase & 1023u) != 0;
-    *c.abort = ((*reinterpret_cast<volatile unsigned int*>(&g_idx_status) & MLA_DEVICE_TIMEOUT) || misaligned) ? 1u : 0u;
+    *c.abort = misaligned ? 1u : 0u;
     if (misaligned) atomicOr(&g_idx_status, MLA_DEVICE_TIMEOUT);
     for (int i = 0; i < kMaxStages; ++i) {
       mbar_init(c.bar(kBarFull + i), 1);
@@ -216,9 +227,9 @@ idx_scores_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         }
         // every copy issued here lands before the CTA may exit, even after an abort
         volatile uint32_t never = 0;
-        mbar_wait<false>(c.bar(kBarQReady), 0, &never, kWaitLimitNs);
+        mbar_wait<false>(c.bar(kBarQReady), 0, &never, c.wait_ns > kDrainWaitNs ? c.wait_ns : kDrainWaitNs);
         for (int i = issued > p.stages ? issued - p.stages : 0; i < issued; ++i)
-          mbar_wait<false>(c.bar(kBarFull + i % p.stages), (i / p.stages) & 1, &never, kWaitLimitNs);
+          mbar_wait<false>(c.bar(kBarFull + i % p.stages), (i / p.stages) & 1, &never, c.wait_ns > kDrainWaitNs ? c.wait_ns : kDrainWaitNs);
       }
       __syncwarp();
     } else if (warp == 1) {
@@ -246,7 +257,7 @@ idx_scores_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         // no MMA may still run when TMEM is released, even after an abort
         umma_commit(c.bar(kBarFinal));
         volatile uint32_t never = 0;
-        mbar_wait<false>(c.bar(kBarFinal), 0, &never, kWaitLimitNs);
+        mbar_wait<false>(c.bar(kBarFinal), 0, &never, c.wait_ns > kDrainWaitNs ? c.wait_ns : kDrainWaitNs);
       }
       __syncwarp();
     } else if (warp < kEpiWarp0) {
@@ -805,6 +816,7 @@ mla_status launch_scores(const mla_indexer_dims& d, int dev, const void* q, cons
   uint32_t cols = 32;
   while (cols < static_cast<uint32_t>(sp.n_acc * sp.N)) cols <<= 1;
   sp.tmem_cols = cols;
+  sp.wait_ns = mlasp::host_wait_limit_ns();
   // about one wave: split each sequence's tiles over SMs / B CTAs
   const int per_b = g_sm_count[dev] / d.B > 1 ? g_sm_count[dev] / d.B : 1;
   sp.tiles_per_cta = (d.max_blocks_per_seq + per_b - 1) / per_b;

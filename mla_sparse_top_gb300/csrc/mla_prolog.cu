@@ -45,6 +45,10 @@
 #include "../../include/mla_prolog.h"
 #include "ptx.cuh"
 
+namespace mlasp {
+unsigned long long host_wait_limit_ns();  // the library's wait bound (mla_sparse_set_wait_limit_ns)
+}
+
 namespace mlapro {
 using namespace mlasp;
 
@@ -305,7 +309,9 @@ constexpr int kGemmRing = kGemmMaxStages * kGemmStageBytes;  // 192 KB
 constexpr int kGemmOffBars = kGemmRing;
 constexpr int kGemmBars = 2 * kGemmMaxStages + 4 + 1;  // full, empty, acc full [2], acc empty [2], final
 constexpr int kGemmSmem = kGemmOffBars + kGemmBars * 8 + 16 + 1024;  // + slack to align the base to 1024
-constexpr uint64_t kGemmWaitNs = 500ull * 1000ull * 1000ull;
+// Waits that only let MMAs already in flight complete before the CTA exits are
+// never cut shorter than this, whatever the configured bound.
+constexpr uint64_t kGemmDrainNs = 500ull * 1000ull * 1000ull;
 
 struct GemmJob {
   int F, kb, splits, batches, f_tiles, t_tiles, units;
@@ -318,6 +324,7 @@ struct GemmParams {
   GemmJob job[2];
   int njobs, T, total_units;
   int fsub;  // 128-feature blocks per unit: 2 (at most 128 tokens) or 1; token halves per unit: 3 - fsub
+  unsigned long long wait_ns;  // bound of every wait (mla_sparse_set_wait_limit_ns)
 };
 
 struct GemmUnit {
@@ -398,7 +405,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap w0, const __grid_constant__ CUte
         const int nt = (tsub == 2 && t0 + 128 < p.T) ? 2 : 1;  // token halves loaded
         for (int kb = g.k0; kb < g.k1 && ok; ++kb, ++it) {
           const int st = it % nst;
-          ok = mbar_wait<false>(bar(kEmpty + st), ((it / nst) & 1) ^ 1, abort, kGemmWaitNs);
+          ok = mbar_wait<false>(bar(kEmpty + st), ((it / nst) & 1) ^ 1, abort, p.wait_ns);
           if (!ok) break;
           const uint32_t stage = sb + st * kGemmStageBytes;
           const uint32_t fb = bar(kFull + st);
@@ -421,13 +428,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap w0, const __grid_constant__ CUte
         const GemmUnit g = unit_of(p, u);
         const int nt = (tsub == 2 && g.tt * 256 + 128 < p.T) ? 2 : 1;
         const int a = lu & 1;
-        ok = mbar_wait<false>(bar(kAccEmpty + a), ((lu >> 1) & 1) ^ 1, abort, kGemmWaitNs);
+        ok = mbar_wait<false>(bar(kAccEmpty + a), ((lu >> 1) & 1) ^ 1, abort, p.wait_ns);
         if (!ok) break;
         tc_fence_after();
         const uint32_t d = tmem + 256 * a;
         for (int kb = g.k0; kb < g.k1; ++kb, ++it) {
           const int st = it % nst;
-          ok = mbar_wait<false>(bar(kFull + st), (it / nst) & 1, abort, kGemmWaitNs);
+          ok = mbar_wait<false>(bar(kFull + st), (it / nst) & 1, abort, p.wait_ns);
           if (!ok) break;
           tc_fence_after();
           const uint32_t stage = sb + st * kGemmStageBytes;
@@ -462,7 +469,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap w0, const __grid_constant__ CUte
       }
       umma_commit(bar(kFinal));
       volatile uint32_t never = 0;
-      mbar_wait<false>(bar(kFinal), 0, &never, kGemmWaitNs);
+      mbar_wait<false>(bar(kFinal), 0, &never, p.wait_ns > kGemmDrainNs ? p.wait_ns : kGemmDrainNs);
     }
     __syncwarp();
   } else {
@@ -472,7 +479,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap w0, const __grid_constant__ CUte
       const GemmUnit g = unit_of(p, u);
       const GemmJob& J = p.job[g.j];
       const int a = lu & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait<false>(bar(kAccFull + a), (lu >> 1) & 1, abort, kGemmWaitNs))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait<false>(bar(kAccFull + a), (lu >> 1) & 1, abort, p.wait_ns))) break;
       tc_fence_after();
       const uint32_t lanes = static_cast<uint32_t>(32 * warp) << 16;
       {
@@ -689,6 +696,7 @@ cudaError_t launch_chained(void (*kernel)(KArgs...), unsigned grid, unsigned blo
 mla_status launch_gemm(const CUtensorMap& w0, const CUtensorMap& x0, const CUtensorMap& w1, const CUtensorMap& x1,
                        mlapro::GemmParams gp, int sms, cudaStream_t s, const char* what) {
   gp.total_units = gp.job[0].units + (gp.njobs > 1 ? gp.job[1].units : 0);
+  gp.wait_ns = mlasp::host_wait_limit_ns();
   gp.fsub = mlapro::fsub_of(gp.T);
   const unsigned grid = static_cast<unsigned>(std::min(gp.total_units, sms));
   PRO_CUDA(launch_chained(mlapro::gemm_kernel, grid, mlapro::kGemmThreads, mlapro::kGemmSmem, s, w0, x0, w1, x1, gp),

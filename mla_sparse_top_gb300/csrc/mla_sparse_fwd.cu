@@ -1329,6 +1329,11 @@ cudaError_t prepare_kernel(int dev) {
 
 }  // namespace
 
+namespace mlasp {
+// The bound of every device-side wait, read by each of the library's launches.
+unsigned long long host_wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+}  // namespace mlasp
+
 extern "C" {
 
 int32_t mla_sparse_abi_version(void) { return 202; }

@@ -7,7 +7,9 @@ MLA_DEVICE_TIMEOUT in the device status word.  Here the bound is cut to 1 us,
 far below the first gather's latency, so a wait runs out on purpose (nothing
 on the GPU is made to fail: the work is only slower than the bound).  The
 status must show the timeout; after clearing it and restoring the bound, the
-next call on the same inputs must match the oracle.
+next call on the same inputs must match the oracle.  The Lightning Indexer's
+score kernel and the MLA Prolog's product kernel take the same bound: for them
+the call after the timeout must repeat, bit for bit, a call made before it.
 """
 import numpy as np
 import pytest
@@ -53,3 +55,75 @@ def test_a_wait_that_runs_out_is_reported_and_the_next_call_is_exact(name, B, to
     assert_out_close(out, ref_out, f"{name} B={B} int8={kv_int8} after a timeout")
     assert_lse_close(lse, ref_lse, f"{name} B={B} int8={kv_int8} after a timeout")
     assert np.isfinite(out).all()
+
+
+def _flush_l2():
+    # a write larger than L2, so that the next call's first loads come from HBM
+    torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda").fill_(1.0)
+    torch.cuda.synchronize()
+
+
+def test_indexer_wait_that_runs_out_is_reported_and_the_next_call_is_identical():
+    """The Lightning Indexer's score kernel takes the same bound: a 1 us bound
+    makes its waits run out, the status shows it, and after restoring the
+    bound the next call gives the same selection bit for bit."""
+    import mla_sparse_top_gb300 as mla
+    inp = workloads.INDEXER_NAMED["indexer_decode"]()
+    dev = workloads.indexer_to_device(inp)
+    dims = mla.indexer_dims_from_workload(inp["dims"])
+    ws = torch.empty(mla.mla_indexer_workspace_bytes(dims), dtype=torch.uint8, device="cuda")
+
+    def call():
+        dev["topk_idx"].fill_(-7)
+        mla.mla_indexer_topk(dev["q"], dev["w"], dev["k_cache"], dev["block_table"], dev["act_seqs"],
+                             dev["topk_idx"], ws, dims=dims)
+        return mla.indexer_device_status(clear=True), dev["topk_idx"].cpu().numpy().copy()
+
+    status, ref = call()
+    assert status == 0
+    _flush_l2()
+    mla.set_wait_limit_ns(1000)
+    try:
+        status, _ = call()
+    finally:
+        mla.set_wait_limit_ns(mla.DEFAULT_WAIT_LIMIT_NS)
+    assert status & mla.MLA_DEVICE_TIMEOUT, f"status {status:#x}: no wait ran out under a 1 us bound"
+    status, again = call()
+    assert status == 0
+    np.testing.assert_array_equal(again, ref)
+
+
+def test_prolog_wait_that_runs_out_is_reported_and_the_next_call_is_identical():
+    """The MLA Prolog's product kernel takes the same bound (decode size: its
+    weights, 123 MB, stream from HBM)."""
+    import mla_sparse_top_gb300 as mla
+    inp = workloads.PROLOG_NAMED["prolog_decode"]()
+    dev = workloads.prolog_to_device(inp)
+    d = inp["dims"]
+    T, H = d["T"], d["n_heads"]
+    q_nope = torch.empty((T, H, 512), dtype=torch.bfloat16, device="cuda")
+    q_rope = torch.empty((T, H, 64), dtype=torch.bfloat16, device="cuda")
+    dims = mla.prolog_dims(dev["x"], dev["wq_a"], dev["wq_b"], dev["kv_nope"])
+    ws = torch.empty(mla.mla_prolog_workspace_bytes(dims), dtype=torch.uint8, device="cuda")
+
+    def call():
+        q_nope.fill_(float("nan"))
+        mla.mla_prolog(dev["x"], dev["wq_a"], dev["gamma_cq"], dev["wq_b"], dev["w_uk"], dev["wkv"], dev["gamma_ckv"],
+                       dev["cos"], dev["sin"], dev["cache_index"], q_nope, q_rope, dev["kv_nope"], dev["kv_rope"],
+                       dev["kv_scales"], ws, dims=dims)
+        return (mla.prolog_device_status(clear=True), q_nope.view(torch.int16).cpu().numpy().copy(),
+                q_rope.view(torch.int16).cpu().numpy().copy())
+
+    status, ref_n, ref_r = call()
+    assert status == 0
+    _flush_l2()
+    mla.set_wait_limit_ns(1000)
+    try:
+        status, _, _ = call()
+    finally:
+        mla.set_wait_limit_ns(mla.DEFAULT_WAIT_LIMIT_NS)
+    assert status & mla.MLA_DEVICE_TIMEOUT, f"status {status:#x}: no wait ran out under a 1 us bound"
+    status, n2, r2 = call()
+    assert status == 0
+    np.testing.assert_array_equal(n2, ref_n)
+    np.testing.assert_array_equal(r2, ref_r)

@@ -19,8 +19,9 @@ step = one mla_prolog call (five launches of the library's kernels: three of
 its tcgen05 product kernel and two row kernels).
 
 Prints one JSON line (rank 0).  ``value`` is microseconds per call (the
-device-timed kernel, CUDA events on the launching stream, L2 flushed by a
-256 MiB write between timed calls); ``e2e`` is the same call made through the
+device-timed kernel, CUDA events on the launching stream, L2 flushed between
+timed calls by a 256 MiB write and a 256 MiB read of another buffer, so each
+call starts cold and clean); ``e2e`` is the same call made through the
 C ABI with the step's inputs copied from pinned host memory and the outputs
 copied back inside the timed region.  For the attention workloads it is
 measured two ways, in order on one stream per step and as a pipelined serving
@@ -305,7 +306,7 @@ def run_config(workload, d, world, window=None):
                     f"{'int8' if d['kv_int8'] else 'bf16'} paged cache ({d['num_blocks']} blocks of 128)",
         "B": d["B"], "S1": d["S1"], "n_q": d["n_q"], "topk": d["topk"],
         "kv_dtype": "int8" if d["kv_int8"] else "bf16",
-        "l2": "flushed between timed calls by a 256 MiB write (outside the per-call events)",
+        "l2": L2_NOTE,
         "launch": "a bounded GPU spin precedes each timed call, so its events time the device, not the host launch",
         "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
     }
@@ -328,6 +329,30 @@ def spin_gpu():
     (which ``e2e`` includes)."""
     import torch
     torch.cuda._sleep(SPIN_CYCLES)
+
+
+class L2Flush:
+    """The flush between timed calls (outside their events): a 256 MiB write
+    (twice L2), then a 256 MiB read of another buffer.  The write evicts every
+    line the previous call left; the read then evicts the write's own dirty
+    lines, so their write-back happens here and not inside the next timed
+    call, which starts with none of its inputs in L2 and only clean lines.
+    ``w`` alone is the write used inside the pipelined serving loop's steps."""
+
+    def __init__(self):
+        import torch
+        n = 256 * 1024 * 1024 // 4
+        self.w = torch.empty(n, dtype=torch.float32, device="cuda")
+        self.r = torch.ones(n, dtype=torch.float32, device="cuda")
+
+    def __call__(self, i):
+        import torch
+        self.w.fill_(float(i))
+        torch.amax(self.r)
+
+
+L2_NOTE = ("flushed between timed calls (outside the per-call events) by a 256 MiB write and then a 256 MiB read "
+           "of another buffer: no input left in L2, and no dirty lines whose write-back would land in the call")
 
 
 # ------------------------------------------------------------------ clocks
@@ -509,9 +534,9 @@ def main():
                                     b["topk_idx"], b["block_table"], b["act_seqs"], b["out"], b["lse"],
                                     softmax_scale=inp["softmax_scale"], mode=mode, dims=dims, stream=stream)
 
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    flush = L2Flush()
     for i in range(max(3, args.warmup)):
-        flush.fill_(float(i))
+        flush(i)
         launch()
     torch.cuda.synchronize()
     if mla.device_status(clear=True):
@@ -528,7 +553,7 @@ def main():
     clocks.mark_on()
     launches0 = mla.launch_count()
     for i in range(args.steps):
-        flush.fill_(float(i))
+        flush(i)
         spin_gpu()
         starts[i].record(stream)
         launch()
@@ -566,7 +591,7 @@ def main():
     e_s = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
     e_e = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
     for i in range(e2e_steps + 2):
-        flush.fill_(float(i))
+        flush(i)
         k = i - 2
         if k >= 0:
             e_s[k].record(stream)
@@ -579,7 +604,7 @@ def main():
             e_e[k].record(stream)
     torch.cuda.synchronize()
     e2e_ms = [s.elapsed_time(e) for s, e in zip(e_s, e_e)]
-    pipe_us = pipelined_e2e(stream, flush, launch, dev, host_in, e2e_steps)
+    pipe_us = pipelined_e2e(stream, flush.w, launch, dev, host_in, e2e_steps)
     clock_summary = clocks.stop()
 
     # median of the cold-L2 calls (the headline); mean and the warm back-to-back figure beside it
@@ -610,7 +635,7 @@ def main():
             "data": "synthetic",
             "config": run_config(args.workload, d, world, inp.get("window")),
             "timing": {"statistic": "median of cold-L2 calls", "mean_us": round(mean_us, 3),
-                       "warm_back_to_back_us": round(warm_us, 3), "l2_flush": "256 MiB write between calls"},
+                       "warm_back_to_back_us": round(warm_us, 3), "l2_flush": "256 MiB write, then 256 MiB read, between calls"},
             "gathered_kv_tbps": round(counts["gathered_bytes"] * world / (us * 1e-6) / 1e12, 4),
             "tflops": round(tflops * world, 2),
             "roofline_us": round(roofline_us, 3),
@@ -670,7 +695,7 @@ def indexer_config(workload, d, world):
         "workload": f"{workload}: B={d['B']} S1={d['S1']} H={d['n_heads']} D={d['head_dim']} topk={d['topk']} "
                     f"bf16 paged key cache ({d['num_blocks']} blocks of 128)",
         "B": d["B"], "S1": d["S1"], "n_heads": d["n_heads"], "head_dim": d["head_dim"], "topk": d["topk"],
-        "l2": "flushed between timed calls by a 256 MiB write (outside the per-call events)",
+        "l2": L2_NOTE,
         "launch": "a bounded GPU spin precedes each timed call, so its events time the device, not the host launch",
         "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
     }
@@ -744,9 +769,9 @@ def main_indexer(args, world, rank, local_rank):
     def launch_select():
         mla.mla_indexer_select(scores, dev["act_seqs"], dev["topk_idx"], dims=dims, stream=stream)
 
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    flush = L2Flush()
     for i in range(max(3, args.warmup)):
-        flush.fill_(float(i))
+        flush(i)
         launch_scores()
         launch_select()
     torch.cuda.synchronize()
@@ -767,7 +792,7 @@ def main_indexer(args, world, rank, local_rank):
     torch.cuda.synchronize()
     clocks.mark_on()
     for i in range(args.steps):
-        flush.fill_(float(i))
+        flush(i)
         spin_gpu()
         st_ev[i][0].record(stream)
         launch_both()
@@ -780,7 +805,7 @@ def main_indexer(args, world, rank, local_rank):
     # each kernel on its own (an event between them), for the per-kernel roofline
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     for i in range(args.steps):
-        flush.fill_(float(i))
+        flush(i)
         spin_gpu()
         ev[i][0].record(stream)
         launch_scores()
@@ -801,7 +826,7 @@ def main_indexer(args, world, rank, local_rank):
     e_s = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
     e_e = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
     for i in range(e2e_steps + 2):
-        flush.fill_(float(i))
+        flush(i)
         k = i - 2
         if k >= 0:
             e_s[k].record(stream)
@@ -924,7 +949,7 @@ def cache_write_config(workload, d, world):
         "workload": f"{workload}: T={d['T']} new rows into a {'INT8' if d['kv_int8'] else 'bf16'} paged cache of "
                     f"{d['num_blocks']} blocks of 128",
         "T": d["T"], "kv_dtype": "int8" if d["kv_int8"] else "bf16",
-        "l2": "flushed between timed calls by a 256 MiB write (outside the per-call events)",
+        "l2": L2_NOTE,
         "launch": "a bounded GPU spin precedes each timed call, so its events time the device, not the host launch",
         "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
     }
@@ -962,9 +987,9 @@ def main_cache_write(args, world, rank, local_rank):
         mla.mla_cache_write(dev["k_nope"], dev["k_rope"], dev["cache_index"], dev["kv_nope"], dev["kv_rope"],
                             dev["kv_scales"], stream=stream)
 
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    flush = L2Flush()
     for i in range(max(3, args.warmup)):
-        flush.fill_(float(i))
+        flush(i)
         launch()
     torch.cuda.synchronize()
     if mla.cache_device_status(clear=True):
@@ -979,7 +1004,7 @@ def main_cache_write(args, world, rank, local_rank):
     torch.cuda.synchronize()
     clocks.mark_on()
     for i in range(args.steps):
-        flush.fill_(float(i))
+        flush(i)
         spin_gpu()
         starts[i].record(stream)
         launch()
@@ -998,7 +1023,7 @@ def main_cache_write(args, world, rank, local_rank):
     e_s = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
     e_e = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
     for i in range(e2e_steps + 2):
-        flush.fill_(float(i))
+        flush(i)
         k = i - 2
         if k >= 0:
             e_s[k].record(stream)
@@ -1091,7 +1116,7 @@ def prolog_config(workload, d, world):
                     f"cache of {d['num_blocks']} blocks of 128",
         "T": d["T"], "hidden": d["hidden"], "q_lora": d["q_lora"], "n_heads": d["n_heads"],
         "kv_dtype": "int8" if d["kv_int8"] else "bf16",
-        "l2": "flushed between timed calls by a 256 MiB write (outside the per-call events)",
+        "l2": L2_NOTE,
         "launch": "a bounded GPU spin precedes each timed call, so its events time the device, not the host launch",
         "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
     }
@@ -1122,9 +1147,9 @@ def main_prolog(args, world, rank, local_rank):
                        dev["gamma_ckv"], dev["cos"], dev["sin"], dev["cache_index"], q_nope, q_rope, dev["kv_nope"],
                        dev["kv_rope"], dev["kv_scales"], ws, dims=dims, stream=stream)
 
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    flush = L2Flush()
     for i in range(max(3, args.warmup)):
-        flush.fill_(float(i))
+        flush(i)
         launch()
     torch.cuda.synchronize()
     if mla.prolog_device_status(clear=True):
@@ -1139,7 +1164,7 @@ def main_prolog(args, world, rank, local_rank):
     torch.cuda.synchronize()
     clocks.mark_on()
     for i in range(args.steps):
-        flush.fill_(float(i))
+        flush(i)
         spin_gpu()
         starts[i].record(stream)
         launch()
@@ -1160,7 +1185,7 @@ def main_prolog(args, world, rank, local_rank):
     e_s = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
     e_e = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
     for i in range(e2e_steps + 2):
-        flush.fill_(float(i))
+        flush(i)
         k = i - 2
         if k >= 0:
             e_s[k].record(stream)

@@ -19,7 +19,7 @@ step = one mla_prolog call (five launches of the library's kernels: three of
 its tcgen05 product kernel and two row kernels).
 
 Prints one JSON line (rank 0).  ``value`` is microseconds per call (the
-device-timed kernel, CUDA events on the launching stream, L2 flushed between
+median over the timed calls, the mean beside it; the device-timed kernel, CUDA events on the launching stream, L2 flushed between
 timed calls by a 256 MiB write and a 256 MiB read of another buffer, so each
 call starts cold and clean); ``e2e`` is the same call made through the
 C ABI with the step's inputs copied from pinned host memory and the outputs
@@ -801,7 +801,9 @@ def main_indexer(args, world, rank, local_rank):
     clocks.mark_off()
     if world > 1:
         dist.barrier()
-    t_step = float(np.mean([e[0].elapsed_time(e[1]) for e in st_ev]) * 1000.0)
+    step_ms = [e[0].elapsed_time(e[1]) for e in st_ev]
+    t_step = float(np.median(step_ms) * 1000.0)
+    mean_step = float(np.mean(step_ms) * 1000.0)
     # each kernel on its own (an event between them), for the per-kernel roofline
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     for i in range(args.steps):
@@ -813,8 +815,8 @@ def main_indexer(args, world, rank, local_rank):
         launch_select()
         ev[i][2].record(stream)
     torch.cuda.synchronize()
-    t_scores = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]) * 1000.0)
-    t_select = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]) * 1000.0)
+    t_scores = float(np.median([e[0].elapsed_time(e[1]) for e in ev]) * 1000.0)
+    t_select = float(np.median([e[1].elapsed_time(e[2]) for e in ev]) * 1000.0)
     status = mla.indexer_device_status(clear=True)
 
     # end to end through the public call with pinned host buffers (the key cache stays resident)
@@ -838,9 +840,10 @@ def main_indexer(args, world, rank, local_rank):
         if k >= 0:
             e_e[k].record(stream)
     torch.cuda.synchronize()
-    e2e_us = float(np.mean([a.elapsed_time(b) for a, b in zip(e_s, e_e)]) * 1000.0)
+    e2e_us = float(np.median([a.elapsed_time(b) for a, b in zip(e_s, e_e)]) * 1000.0)
     clock_summary = clocks.stop()
-    t_step, t_scores, t_select, e2e_us = reduce_max_over_ranks([t_step, t_scores, t_select, e2e_us], device="cuda")
+    t_step, t_scores, t_select, e2e_us, mean_step = reduce_max_over_ranks(
+        [t_step, t_scores, t_select, e2e_us, mean_step], device="cuda")
 
     if rank == 0:
         hbm_gbs, bf16_tf, peak_src = measured_peaks()
@@ -862,6 +865,7 @@ def main_indexer(args, world, rank, local_rank):
             "data": "synthetic",
             "config": indexer_config(args.workload, d, world),
             "kernels_us": {k: round(v, 3) for k, v in per_kernel.items()},
+            "timing": {"statistic": "median of cold-L2 calls", "mean_us": round(mean_step, 3)},
             "roofline": {
                 "bound": "hbm",
                 "achieved": round(achieved, 1),
@@ -1013,7 +1017,9 @@ def main_cache_write(args, world, rank, local_rank):
     clocks.mark_off()
     if world > 1:
         dist.barrier()
-    us = float(np.mean([a.elapsed_time(b) for a, b in zip(starts, ends)]) * 1000.0)
+    call_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    us = float(np.median(call_ms) * 1000.0)
+    mean_us = float(np.mean(call_ms) * 1000.0)
     status = mla.cache_device_status(clear=True)
     # end to end: the new rows and their indices from pinned host memory, then the call; the
     # result is the updated device cache, so nothing is read back but the status word
@@ -1033,9 +1039,9 @@ def main_cache_write(args, world, rank, local_rank):
         if k >= 0:
             e_e[k].record(stream)
     torch.cuda.synchronize()
-    e2e_us = float(np.mean([a.elapsed_time(b) for a, b in zip(e_s, e_e)]) * 1000.0)
+    e2e_us = float(np.median([a.elapsed_time(b) for a, b in zip(e_s, e_e)]) * 1000.0)
     clock_summary = clocks.stop()
-    us, e2e_us = reduce_max_over_ranks([us, e2e_us], device="cuda")
+    us, e2e_us, mean_us = reduce_max_over_ranks([us, e2e_us, mean_us], device="cuda")
     if rank == 0:
         hbm_gbs, _, peak_src = measured_peaks()
         nbytes = cache_write_counts(inp)
@@ -1050,6 +1056,7 @@ def main_cache_write(args, world, rank, local_rank):
                          "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                          else "fallback",
                          "algorithmic_bytes_per_launch": nbytes, "kernel": "cache_write_kernel"},
+            "timing": {"statistic": "median of cold-L2 calls", "mean_us": round(mean_us, 3)},
             "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": 0},
             "gpu_launches": args.steps, "clocks": clock_summary, "device_status": status,
@@ -1173,7 +1180,9 @@ def main_prolog(args, world, rank, local_rank):
     clocks.mark_off()
     if world > 1:
         dist.barrier()
-    us = float(np.mean([a.elapsed_time(b) for a, b in zip(starts, ends)]) * 1000.0)
+    call_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    us = float(np.median(call_ms) * 1000.0)
+    mean_us = float(np.mean(call_ms) * 1000.0)
     status = mla.prolog_device_status(clear=True)
     # end to end: x, cos/sin and the indices from pinned host memory, the call, q_nope and q_rope back
     host_in = {k: dev[k].cpu().pin_memory() for k in ("x", "cos", "sin", "cache_index")}
@@ -1197,9 +1206,9 @@ def main_prolog(args, world, rank, local_rank):
         if k >= 0:
             e_e[k].record(stream)
     torch.cuda.synchronize()
-    e2e_us = float(np.mean([a.elapsed_time(b) for a, b in zip(e_s, e_e)]) * 1000.0)
+    e2e_us = float(np.median([a.elapsed_time(b) for a, b in zip(e_s, e_e)]) * 1000.0)
     clock_summary = clocks.stop()
-    us, e2e_us = reduce_max_over_ranks([us, e2e_us], device="cuda")
+    us, e2e_us, mean_us = reduce_max_over_ranks([us, e2e_us, mean_us], device="cuda")
     if rank == 0:
         hbm_gbs, bf16_tf, peak_src = measured_peaks()
         nbytes, flops = prolog_counts(inp)
@@ -1217,6 +1226,7 @@ def main_prolog(args, world, rank, local_rank):
                          "kernel": "the whole mla_prolog call (gemm_kernel x3 + x_rows_kernel, q_heads_kernel)",
                          "tensor_tflops": round(flops / (us * 1e-6) / 1e12, 1),
                          "tensor_frac_of_bf16_peak": round(flops / (us * 1e-6) / 1e12 / bf16_tf, 4)},
+            "timing": {"statistic": "median of cold-L2 calls", "mean_us": round(mean_us, 3)},
             "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h)},
             "gpu_launches": 5 * args.steps, "clocks": clock_summary,

@@ -19,9 +19,8 @@ step = one mla_prolog call (five launches of the library's kernels: three of
 its tcgen05 product kernel and two row kernels).
 
 Prints one JSON line (rank 0).  ``value`` is microseconds per call (the
-median over the timed calls, the mean beside it; the device-timed kernel, CUDA events on the launching stream, L2 flushed between
-timed calls by a 256 MiB write and a 256 MiB read of another buffer, so each
-call starts cold and clean); ``e2e`` is the same call made through the
+median over the timed calls, the mean beside it; the device-timed kernel, CUDA events on the launching stream, L2 flushed by a
+256 MiB write between timed calls); ``e2e`` is the same call made through the
 C ABI with the step's inputs copied from pinned host memory and the outputs
 copied back inside the timed region.  For the attention workloads it is
 measured two ways, in order on one stream per step and as a pipelined serving
@@ -332,27 +331,19 @@ def spin_gpu():
 
 
 class L2Flush:
-    """The flush between timed calls (outside their events): a 256 MiB write
-    (twice L2), then a 256 MiB read of another buffer.  The write evicts every
-    line the previous call left; the read then evicts the write's own dirty
-    lines, so their write-back happens here and not inside the next timed
-    call, which starts with none of its inputs in L2 and only clean lines.
-    ``w`` alone is the write used inside the pipelined serving loop's steps."""
+    """The flush between timed calls (outside their events): a 256 MiB write,
+    twice L2, which evicts every line the previous call left.  ``w`` is the
+    same write, used inside the pipelined serving loop's steps."""
 
     def __init__(self):
         import torch
-        n = 256 * 1024 * 1024 // 4
-        self.w = torch.empty(n, dtype=torch.float32, device="cuda")
-        self.r = torch.ones(n, dtype=torch.float32, device="cuda")
+        self.w = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
 
     def __call__(self, i):
-        import torch
         self.w.fill_(float(i))
-        torch.amax(self.r)
 
 
-L2_NOTE = ("flushed between timed calls (outside the per-call events) by a 256 MiB write and then a 256 MiB read "
-           "of another buffer: no input left in L2, and no dirty lines whose write-back would land in the call")
+L2_NOTE = "flushed between timed calls by a 256 MiB write (outside the per-call events)"
 
 
 # ------------------------------------------------------------------ clocks
@@ -635,7 +626,7 @@ def main():
             "data": "synthetic",
             "config": run_config(args.workload, d, world, inp.get("window")),
             "timing": {"statistic": "median of cold-L2 calls", "mean_us": round(mean_us, 3),
-                       "warm_back_to_back_us": round(warm_us, 3), "l2_flush": "256 MiB write, then 256 MiB read, between calls"},
+                       "warm_back_to_back_us": round(warm_us, 3), "l2_flush": "256 MiB write between calls"},
             "gathered_kv_tbps": round(counts["gathered_bytes"] * world / (us * 1e-6) / 1e12, 4),
             "tflops": round(tflops * world, 2),
             "roofline_us": round(roofline_us, 3),

@@ -190,6 +190,7 @@ struct Params {
   int cmp_num_blocks, cmp_mbps, cmp_ratio, cmp_topk;
   float scale_log2;
   unsigned long long wait_ns;  // bound of every wait
+  int out32;  // out is 32-byte aligned: the epilogue stores 32 bytes per instruction
 };
 
 struct Ctx {
@@ -272,6 +273,12 @@ __device__ __forceinline__ bool warp_wait_cluster(const Ctx& c, int idx, uint32_
 __device__ __forceinline__ uint4 ldg16(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
 __device__ __forceinline__ void sts16(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+// 32-byte global store (both halves of a 64-byte-aligned pair of uint4 at p, p 32-byte aligned).
+__device__ __forceinline__ void stg32(void* p, uint4 a, uint4 b) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               :: "l"(p), "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
                : "memory");
 }
 __device__ __forceinline__ int lds_s32(uint32_t addr) {
@@ -1084,14 +1091,22 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
       tmem_ld_32x32b_x32(tO + 32 * ch + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
       tmem_wait_ld();
       if (live) {
+        // a warp's 32 heads are 1 KB apart in out, so every store instruction
+        // touches 32 lines: 32-byte stores (when out allows) halve the count
+        uint4 w[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l);
-          w.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l);
-          w.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l);
-          w.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l);
-          op[ch * 4 + k] = w;
+          w[k].x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l);
+          w[k].y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l);
+          w[k].z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l);
+          w[k].w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l);
+        }
+        if (p.out32) {
+#pragma unroll
+          for (int k = 0; k < 8; k += 2) stg32(op + ch * 4 + k, w[k], w[k + 1]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) op[ch * 4 + k] = w[k];
         }
       }
     }
@@ -1435,6 +1450,7 @@ mla_status attn_fwd(const mla_dims* dims, const void* q_nope, const void* q_rope
   p.mbps = d.max_blocks_per_seq;
   p.n_tiles = (d.topk + mlasp::kTileKeys - 1) / mlasp::kTileKeys;
   p.scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634);
+  p.out32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0 ? 1 : 0;
   p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
   // Persistent clusters, as many as run at once.  Whole tokens per cluster by
   // default.  Equal shares of tiles (list mode only) cost a token switch per

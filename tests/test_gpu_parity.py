@@ -240,3 +240,22 @@ def test_rescale_inside_a_later_token_of_the_stream():
     scaled = np.where(nz, q + (4 << 7), q).astype(np.uint16)  # x16, exact in bf16
     inp["q_nope"][160:] = scaled[160:]
     check_full(inp, "rescale in later tokens")
+
+
+def test_output_aligned_to_16_bytes_only():
+    """`out` only has to be 16-byte aligned: the epilogue then stores 16 bytes
+    per instruction instead of 32.  Same bits either way, and the oracle's."""
+    inp = workloads.make_inputs(B=3, S1=2, n_q=128, act_seqs=[3000, 700, 5000], topk=1000, seed=91)
+    dev = to_device(inp)
+    out32, lse32, status = run_gpu(inp, dev=dev)
+    assert status == 0
+    big = torch.empty(dev["out"].numel() + 8, dtype=dev["out"].dtype, device="cuda")
+    dev["out"] = big[8:].view(dev["out"].shape)
+    assert dev["out"].data_ptr() % 32 == 16
+    out16, lse16, status = run_gpu(inp, dev=dev)
+    assert status == 0
+    np.testing.assert_array_equal(out16, out32)
+    np.testing.assert_array_equal(lse16, lse32)
+    ref_out, ref_lse, _ = oracle.forward(inp)
+    assert_out_close(out16, ref_out, "out at a 16-byte offset")
+    assert_lse_close(lse16, ref_lse, "out at a 16-byte offset")

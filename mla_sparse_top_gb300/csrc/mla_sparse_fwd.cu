@@ -1090,24 +1090,49 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
       tmem_ld_32x32b_x32(tO + 32 * ch, *reinterpret_cast<uint32_t(*)[32]>(o));
       tmem_ld_32x32b_x32(tO + 32 * ch + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
       tmem_wait_ld();
-      if (live) {
-        // a warp's 32 heads are 1 KB apart in out, so every store instruction
-        // touches 32 lines: 32-byte stores (when out allows) halve the count
-        uint4 w[8];
+      uint4 w[8];  // this head's 128-byte line of out: dims [32 ch, 32 ch + 64) of the CTA's column half
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          w[k].x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l);
-          w[k].y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l);
-          w[k].z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l);
-          w[k].w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l);
+      for (int k = 0; k < 8; ++k) {
+        w[k].x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l);
+        w[k].y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l);
+        w[k].z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l);
+        w[k].w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l);
+      }
+      if (p.out32) {
+        // A warp's 32 heads lie 1 KB apart in out.  Each group of four lanes
+        // transposes its four lines (2 butterfly stages over 32-byte pieces),
+        // after which lane l of the group holds piece l of the group's e-th
+        // head; the group then writes each head's 128-byte line whole.
+        const int l4 = lane & 3;
+#pragma unroll
+        for (int bit = 1; bit <= 2; bit <<= 1) {
+          const bool b = (l4 & bit) != 0;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (e & bit) continue;
+#pragma unroll
+            for (int v = 0; v < 2; ++v) {
+              uint4& lo = w[2 * e + v];
+              uint4& hi = w[2 * (e + bit) + v];
+              const uint4 snd = b ? lo : hi;
+              uint4 rcv;
+              rcv.x = __shfl_xor_sync(0xffffffffu, snd.x, bit);
+              rcv.y = __shfl_xor_sync(0xffffffffu, snd.y, bit);
+              rcv.z = __shfl_xor_sync(0xffffffffu, snd.z, bit);
+              rcv.w = __shfl_xor_sync(0xffffffffu, snd.w, bit);
+              if (b) lo = rcv; else hi = rcv;
+            }
+          }
         }
-        if (p.out32) {
 #pragma unroll
-          for (int k = 0; k < 8; k += 2) stg32(op + ch * 4 + k, w[k], w[k + 1]);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) op[ch * 4 + k] = w[k];
+        for (int e = 0; e < 4; ++e) {
+          const int dl = (lane & ~3) + e;  // lane of the head written
+          if (q * 32 + dl < p.n_q)
+            stg32(op + static_cast<int64_t>(dl - lane) * 64 + ch * 4 + 2 * l4, w[2 * e], w[2 * e + 1]);
         }
+      } else if (live) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) op[ch * 4 + k] = w[k];
       }
     }
     // O is in registers: the next token's first P.V may overwrite it

@@ -572,27 +572,72 @@ __device__ __forceinline__ bool send_half(const Ctx& c, const uint32_t (&v)[32],
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
-// Q of token qrow / n_q, one sender thread per head h: the CTA's latent dims
-// [128, 256) (128-byte swizzled rows of 64 dims, head h at row h of chunk
-// (d - 128) / 64) and its 32 rope dims go to shared memory by cp.async
-// (zero-filled for heads beyond n_q), then dims [0, 128) to TMEM (the lanes
-// of the thread's quadrant) through registers; then QReady.  The senders load
+// Exchange 32-byte pieces among each group of four lanes so that lane l of
+// the group ends with piece l of the group's e-th line in v[2 e], v[2 e + 1]
+// (two butterfly stages; the same call undoes it).  v holds four 32-byte
+// pieces (eight uint4) per lane.
+__device__ __forceinline__ void transpose4x32(uint4 (&v)[8], int lane) {
+  const int l4 = lane & 3;
+#pragma unroll
+  for (int bit = 1; bit <= 2; bit <<= 1) {
+    const bool b = (l4 & bit) != 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (e & bit) continue;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        uint4& lo = v[2 * e + u];
+        uint4& hi = v[2 * (e + bit) + u];
+        const uint4 snd = b ? lo : hi;
+        uint4 rcv;
+        rcv.x = __shfl_xor_sync(0xffffffffu, snd.x, bit);
+        rcv.y = __shfl_xor_sync(0xffffffffu, snd.y, bit);
+        rcv.z = __shfl_xor_sync(0xffffffffu, snd.z, bit);
+        rcv.w = __shfl_xor_sync(0xffffffffu, snd.w, bit);
+        if (b) lo = rcv; else hi = rcv;
+      }
+    }
+  }
+}
+
+// Q of one token for sender warp q (heads [32 q, 32 q + 32), rows qrow0 ..
+// qrow0 + 31): the CTA's latent dims [128, 256) (128-byte swizzled rows of 64
+// dims, head h at row h of chunk (d - 128) / 64) and its 32 rope dims go to
+// shared memory by cp.async (zero-filled for heads beyond n_q), then dims
+// [0, 128) to TMEM (the lanes of the quadrant) through registers; then
+// QReady.  The heads' rows lie 1 KB apart, so the copies for shared memory
+// assign lanes to whole 128-byte lines rather than to heads (a warp-wide copy
+// then covers 4 lines, not 32); the TMEM dims are loaded per head, into the
+// registers of that head's lane.  The senders load
 // each token's Q as soon as the previous token's score MMAs are complete, so
 // the load overlaps the softmax of that token's last tiles.
-__device__ __forceinline__ void load_q(const Params& p, const Ctx& c, int h, bool live, int64_t qrow, uint32_t tQ) {
-  const uint8_t* qn = reinterpret_cast<const uint8_t*>(p.q_nope) + (qrow * 512 + c.crank * 256) * 2;
-  const uint8_t* qr = reinterpret_cast<const uint8_t*>(p.q_rope) + (qrow * 64 + c.crank * 32) * 2;
-  const uint32_t nb = live ? 16u : 0u;
+__device__ __forceinline__ void load_q(const Params& p, const Ctx& c, int q, int lane, int64_t qrow0, uint32_t tQ) {
+  const uint8_t* qn0 = reinterpret_cast<const uint8_t*>(p.q_nope) + (qrow0 * 512 + c.crank * 256) * 2;
+  const uint8_t* qr0 = reinterpret_cast<const uint8_t*>(p.q_rope) + (qrow0 * 64 + c.crank * 32) * 2;
+  // dims [128, 256): line L = 4 i + lane / 8 of the warp's 64 (head L / 2, chunk L % 2), unit lane % 8
 #pragma unroll
-  for (int ch = 0; ch < 2; ++ch)
+  for (int i = 0; i < 16; ++i) {
+    const int L = 4 * i + (lane >> 3), hh = L >> 1, ch = L & 1, u = lane & 7;
+    const int h = q * 32 + hh;
+    const bool live = h < p.n_q;
+    cp_async_16(c.sbase + kOffQHalf + ch * (kQHalfBytes / 2) + h * 128 + ((u ^ (h & 7)) << 4),
+                live ? static_cast<const void*>(qn0 + static_cast<int64_t>(hh) * 1024 + 256 + ch * 128 + u * 16)
+                     : p.q_nope,
+                live ? 16u : 0u);
+  }
+  // rope: head 8 i + lane / 4, unit lane % 4
 #pragma unroll
-    for (int u = 0; u < 8; ++u)
-      cp_async_16(c.sbase + kOffQHalf + ch * (kQHalfBytes / 2) + h * 128 + ((u ^ (h & 7)) << 4),
-                  live ? static_cast<const void*>(qn + 256 + (8 * ch + u) * 16) : p.q_nope, nb);
-#pragma unroll
-  for (int u = 0; u < 4; ++u)
-    cp_async_16(c.sbase + kOffQRope + rope_unit(h, u), live ? static_cast<const void*>(qr + u * 16) : p.q_rope, nb);
-  // all register loads are issued before the first TMEM store
+  for (int i = 0; i < 4; ++i) {
+    const int hh = 8 * i + (lane >> 2), u = lane & 3;
+    const int h = q * 32 + hh;
+    const bool live = h < p.n_q;
+    cp_async_16(c.sbase + kOffQRope + rope_unit(h, u),
+                live ? static_cast<const void*>(qr0 + static_cast<int64_t>(hh) * 128 + u * 16) : p.q_rope,
+                live ? 16u : 0u);
+  }
+  // dims [0, 128): this lane's head, all register loads issued before the first TMEM store
+  const bool live = q * 32 + lane < p.n_q;
+  const uint8_t* qn = qn0 + static_cast<int64_t>(lane) * 1024;
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
   uint4 qv[16];
 #pragma unroll
@@ -619,7 +664,6 @@ __device__ __forceinline__ void load_q(const Params& p, const Ctx& c, int h, boo
 template <bool kInt8, int kMode>
 __device__ void sender_role(const Params& p, const Ctx& c, int q, int lane) {
   const int h = q * 32 + lane;
-  const bool live = h < p.n_q;
   const uint32_t tQ = c.tmem + (static_cast<uint32_t>(q * 32) << 16) + kTmemQ;
   const uint32_t tR = c.tmem + (static_cast<uint32_t>(q * 32) << 16) + kTmemRegion;
   const uint32_t peer = c.crank ^ 1u;
@@ -627,7 +671,7 @@ __device__ void sender_role(const Params& p, const Ctx& c, int q, int lane) {
   const uint32_t dst = mapa_shared(c.sbase + kOffRecv, peer);
   const uint32_t rbar0 = mapa_shared(c.bar(kBarRecvFull + 0), peer);
   const uint32_t rbar1 = mapa_shared(c.bar(kBarRecvFull + 1), peer);
-  if constexpr (!kInt8) load_q(p, c, h, live, static_cast<int64_t>(token_of<kMode>(p, c, 0)) * p.n_q + h, tQ);
+  if constexpr (!kInt8) load_q(p, c, q, lane, static_cast<int64_t>(token_of<kMode>(p, c, 0)) * p.n_q + q * 32, tQ);
   int m = 0, m_end = seg_end<kMode>(p, c, 0);  // token ordinal and the end of its segment
   // the loop bound comes from shared memory: the two 32-column halves held in
   // registers leave none to spare for it
@@ -648,7 +692,7 @@ __device__ void sender_role(const Params& p, const Ctx& c, int q, int lane) {
       if (!warp_wait(c, kBarQFree, m & 1)) break;
       tc_fence_after();
       ++m;
-      load_q(p, c, h, live, static_cast<int64_t>(token_of<kMode>(p, c, m)) * p.n_q + h, tQ);
+      load_q(p, c, q, lane, static_cast<int64_t>(token_of<kMode>(p, c, m)) * p.n_q + q * 32, tQ);
       m_end = seg_end<kMode>(p, c, m);
     }
   }
@@ -1103,27 +1147,8 @@ __device__ void softmax_role(const Params& p, const Ctx& c, int warp, int lane) 
         // transposes its four lines (2 butterfly stages over 32-byte pieces),
         // after which lane l of the group holds piece l of the group's e-th
         // head; the group then writes each head's 128-byte line whole.
+        transpose4x32(w, lane);
         const int l4 = lane & 3;
-#pragma unroll
-        for (int bit = 1; bit <= 2; bit <<= 1) {
-          const bool b = (l4 & bit) != 0;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            if (e & bit) continue;
-#pragma unroll
-            for (int v = 0; v < 2; ++v) {
-              uint4& lo = w[2 * e + v];
-              uint4& hi = w[2 * (e + bit) + v];
-              const uint4 snd = b ? lo : hi;
-              uint4 rcv;
-              rcv.x = __shfl_xor_sync(0xffffffffu, snd.x, bit);
-              rcv.y = __shfl_xor_sync(0xffffffffu, snd.y, bit);
-              rcv.z = __shfl_xor_sync(0xffffffffu, snd.z, bit);
-              rcv.w = __shfl_xor_sync(0xffffffffu, snd.w, bit);
-              if (b) lo = rcv; else hi = rcv;
-            }
-          }
-        }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int dl = (lane & ~3) + e;  // lane of the head written

@@ -600,20 +600,15 @@ __device__ __forceinline__ void transpose4x32(uint4 (&v)[8], int lane) {
   }
 }
 
-// Q of one token for sender warp q (heads [32 q, 32 q + 32), rows qrow0 ..
-// qrow0 + 31): the CTA's latent dims [128, 256) (128-byte swizzled rows of 64
-// dims, head h at row h of chunk (d - 128) / 64) and its 32 rope dims go to
-// shared memory by cp.async (zero-filled for heads beyond n_q), then dims
-// [0, 128) to TMEM (the lanes of the quadrant) through registers; then
-// QReady.  The heads' rows lie 1 KB apart, so the copies for shared memory
-// assign lanes to whole 128-byte lines rather than to heads (a warp-wide copy
-// then covers 4 lines, not 32); the TMEM dims are loaded per head, into the
-// registers of that head's lane.  The senders load
-// each token's Q as soon as the previous token's score MMAs are complete, so
-// the load overlaps the softmax of that token's last tiles.
-__device__ __forceinline__ void load_q(const Params& p, const Ctx& c, int q, int lane, int64_t qrow0, uint32_t tQ) {
-  const uint8_t* qn0 = reinterpret_cast<const uint8_t*>(p.q_nope) + (qrow0 * 512 + c.crank * 256) * 2;
-  const uint8_t* qr0 = reinterpret_cast<const uint8_t*>(p.q_rope) + (qrow0 * 64 + c.crank * 32) * 2;
+// The shared-memory part of one token's Q for the 32 heads of TMEM lane
+// quadrant q (qn0, qr0: the quadrant's first head row, this CTA's dims):
+// latent dims [128, 256) as 128-byte swizzled rows of 64 dims (head h at row
+// h of chunk (d - 128) / 64) and the 32 rope dims, by cp.async, zero-filled
+// for heads beyond n_q.  Lanes take whole 128-byte lines, not heads: the
+// heads' rows lie 1 KB apart, so a warp-wide copy covers 4 lines (rope: 8
+// half lines) instead of 32 pieces.
+__device__ __forceinline__ void copy_q_smem(const Params& p, const Ctx& c, int q, int lane, const uint8_t* qn0,
+                                            const uint8_t* qr0) {
   // dims [128, 256): line L = 4 i + lane / 8 of the warp's 64 (head L / 2, chunk L % 2), unit lane % 8
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
@@ -635,6 +630,23 @@ __device__ __forceinline__ void load_q(const Params& p, const Ctx& c, int q, int
                 live ? static_cast<const void*>(qr0 + static_cast<int64_t>(hh) * 128 + u * 16) : p.q_rope,
                 live ? 16u : 0u);
   }
+}
+
+// Q of one token for sender warp q (heads [32 q, 32 q + 32), rows qrow0 ..
+// qrow0 + 31): the CTA's latent dims [128, 256) (128-byte swizzled rows of 64
+// dims, head h at row h of chunk (d - 128) / 64) and its 32 rope dims go to
+// shared memory by cp.async (zero-filled for heads beyond n_q), then dims
+// [0, 128) to TMEM (the lanes of the quadrant) through registers; then
+// QReady.  The heads' rows lie 1 KB apart, so the copies for shared memory
+// assign lanes to whole 128-byte lines rather than to heads (a warp-wide copy
+// then covers 4 lines, not 32); the TMEM dims are loaded per head, into the
+// registers of that head's lane.  The senders load
+// each token's Q as soon as the previous token's score MMAs are complete, so
+// the load overlaps the softmax of that token's last tiles.
+__device__ __forceinline__ void load_q(const Params& p, const Ctx& c, int q, int lane, int64_t qrow0, uint32_t tQ) {
+  const uint8_t* qn0 = reinterpret_cast<const uint8_t*>(p.q_nope) + (qrow0 * 512 + c.crank * 256) * 2;
+  const uint8_t* qr0 = reinterpret_cast<const uint8_t*>(p.q_rope) + (qrow0 * 64 + c.crank * 32) * 2;
+  copy_q_smem(p, c, q, lane, qn0, qr0);
   // dims [0, 128): this lane's head, all register loads issued before the first TMEM store
   const bool live = q * 32 + lane < p.n_q;
   const uint8_t* qn = qn0 + static_cast<int64_t>(lane) * 1024;
@@ -807,54 +819,46 @@ __device__ void mma_role(const Params& p, const Ctx& c) {
 }
 
 // ------------------------------------------------------------------ softmax warps
-// INT8 instantiations: Q loaded by the softmax warps themselves (two threads
-// per head), measured faster there than the sender-side load above.
-// Q of token qrow / n_q: latent dims [128 half, 128 half + 128) of the CTA's
-// 256 (the lower half to TMEM, the upper half to shared memory as 128-byte
-// swizzled rows of 64 dims, head h at row h of chunk (d - 128) / 64) and the
-// CTA's rope dims; then QReady.
+// INT8 instantiations: Q of token qrow / n_q loaded by the softmax warps
+// (measured faster there than on the senders, whose registers the INT8
+// kernels cannot spare).  Warps of column half 0 put the CTA's latent dims [0, 128) of their head
+// into TMEM (per head, through registers); warps of column half 1 copy their
+// quadrant's latent dims [128, 256) and all four rope units into shared
+// memory by cp.async, lanes assigned to whole 128-byte lines (the heads' rows
+// lie 1 KB apart); then QReady.
 __device__ __forceinline__ void load_q_softmax(const Params& p, const Ctx& c, int h, int half, bool live,
                                                int64_t qrow, uint32_t tQ) {
-  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  {
-    // All loads are issued before the first store: a shared-memory or TMEM store
-    // (inline asm that may touch memory) would otherwise hold back every later
-    // load behind the previous one's full latency.
-    const uint8_t* qn = reinterpret_cast<const uint8_t*>(p.q_nope) + (qrow * 512 + c.crank * 256 + half * 128) * 2;
-    // Q rope: this CTA's 32 dims [32 crank, 32 crank + 32), units 2 half, 2 half + 1
-    const uint8_t* qr = reinterpret_cast<const uint8_t*>(p.q_rope) + (qrow * 64 + c.crank * 32 + half * 16) * 2;
-    uint4 qv[16], rv[2];
+  const int lane = h & 31, q = h >> 5;
+  if (half == 0) {
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    const uint8_t* qn = reinterpret_cast<const uint8_t*>(p.q_nope) + (qrow * 512 + c.crank * 256) * 2;
+    // all loads are issued before the first TMEM store (inline asm that may
+    // touch memory would otherwise hold back every later load)
+    uint4 qv[16];
 #pragma unroll
     for (int u = 0; u < 16; ++u) qv[u] = live ? ldg16(qn + u * 16) : zero;
 #pragma unroll
-    for (int u = 0; u < 2; ++u) rv[u] = live ? ldg16(qr + u * 16) : zero;
-    if (half == 0) {
+    for (int ch = 0; ch < 2; ++ch) {
+      uint32_t w[32];
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t w[32];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          w[4 * u + 0] = qv[8 * ch + u].x;
-          w[4 * u + 1] = qv[8 * ch + u].y;
-          w[4 * u + 2] = qv[8 * ch + u].z;
-          w[4 * u + 3] = qv[8 * ch + u].w;
-        }
-        tmem_st_32x32b_x32(tQ + 32 * ch, w);
+      for (int u = 0; u < 8; ++u) {
+        w[4 * u + 0] = qv[8 * ch + u].x;
+        w[4 * u + 1] = qv[8 * ch + u].y;
+        w[4 * u + 2] = qv[8 * ch + u].z;
+        w[4 * u + 3] = qv[8 * ch + u].w;
       }
-    } else {
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch)
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          sts16(c.sbase + kOffQHalf + ch * (kQHalfBytes / 2) + h * 128 + ((u ^ (h & 7)) << 4), qv[8 * ch + u]);
+      tmem_st_32x32b_x32(tQ + 32 * ch, w);
     }
-#pragma unroll
-    for (int u = 0; u < 2; ++u) sts16(c.sbase + kOffQRope + rope_unit(h, 2 * half + u), rv[u]);
-    fence_proxy_async_smem();
-    tmem_wait_st();
-    tc_fence_before();
-    mbar_arrive(c.bar(kBarQReady));
+  } else {
+    const int64_t qrow0 = qrow - lane;
+    copy_q_smem(p, c, q, lane, reinterpret_cast<const uint8_t*>(p.q_nope) + (qrow0 * 512 + c.crank * 256) * 2,
+                reinterpret_cast<const uint8_t*>(p.q_rope) + (qrow0 * 64 + c.crank * 32) * 2);
   }
+  cp_async_wait_all();
+  fence_proxy_async_smem();  // cp.async data -> tensor-core reads
+  tmem_wait_st();
+  tc_fence_before();
+  mbar_arrive(c.bar(kBarQReady));
 }
 
 // ------------------------------------------------------------------ cut tokens

@@ -821,8 +821,9 @@ __device__ void mma_role(const Params& p, const Ctx& c) {
 // ------------------------------------------------------------------ softmax warps
 // INT8 instantiations: Q of token qrow / n_q loaded by the softmax warps
 // (measured faster there than on the senders, whose registers the INT8
-// kernels cannot spare).  Warps of column half 0 put the CTA's latent dims [0, 128) of their head
-// into TMEM (per head, through registers); warps of column half 1 copy their
+// kernels cannot spare).  Warps of column half 0 put the CTA's latent dims
+// [0, 128) of their heads into TMEM (loaded line-major by groups of four
+// lanes, transposed back to one head per lane); warps of column half 1 copy their
 // quadrant's latent dims [128, 256) and all four rope units into shared
 // memory by cp.async, lanes assigned to whole 128-byte lines (the heads' rows
 // lie 1 KB apart); then QReady.
@@ -830,22 +831,34 @@ __device__ __forceinline__ void load_q_softmax(const Params& p, const Ctx& c, in
                                                int64_t qrow, uint32_t tQ) {
   const int lane = h & 31, q = h >> 5;
   if (half == 0) {
+    // latent dims [0, 128): loaded line-major (32-byte piece lane % 4 of each
+    // line of the four-lane group's heads), then transposed back to one head
+    // per lane; all loads are issued before the first TMEM store (inline asm
+    // that may touch memory would otherwise hold back every later load)
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-    const uint8_t* qn = reinterpret_cast<const uint8_t*>(p.q_nope) + (qrow * 512 + c.crank * 256) * 2;
-    // all loads are issued before the first TMEM store (inline asm that may
-    // touch memory would otherwise hold back every later load)
-    uint4 qv[16];
+    const int64_t qrow0 = qrow - lane;
+    const uint8_t* qn0 = reinterpret_cast<const uint8_t*>(p.q_nope) + (qrow0 * 512 + c.crank * 256) * 2;
+    const int g4 = lane & ~3, l4 = lane & 3;
+    uint4 qv[2][8];
 #pragma unroll
-    for (int u = 0; u < 16; ++u) qv[u] = live ? ldg16(qn + u * 16) : zero;
+    for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const bool hlive = q * 32 + g4 + e < p.n_q;
+        const uint8_t* src = qn0 + static_cast<int64_t>(g4 + e) * 1024 + ch * 128 + l4 * 32;
+        qv[ch][2 * e] = hlive ? ldg16(src) : zero;
+        qv[ch][2 * e + 1] = hlive ? ldg16(src + 16) : zero;
+      }
 #pragma unroll
     for (int ch = 0; ch < 2; ++ch) {
+      transpose4x32(qv[ch], lane);
       uint32_t w[32];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        w[4 * u + 0] = qv[8 * ch + u].x;
-        w[4 * u + 1] = qv[8 * ch + u].y;
-        w[4 * u + 2] = qv[8 * ch + u].z;
-        w[4 * u + 3] = qv[8 * ch + u].w;
+        w[4 * u + 0] = qv[ch][u].x;
+        w[4 * u + 1] = qv[ch][u].y;
+        w[4 * u + 2] = qv[ch][u].z;
+        w[4 * u + 3] = qv[ch][u].w;
       }
       tmem_st_32x32b_x32(tQ + 32 * ch, w);
     }

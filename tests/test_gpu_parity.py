@@ -120,10 +120,14 @@ def test_early_prefill_positions_fewer_than_topk():
     check_full(inp, "early prefill")
 
 
-@pytest.mark.parametrize("n_q", [1, 16, 100])
-def test_head_counts(n_q):
-    inp = workloads.make_inputs(B=2, S1=1, n_q=n_q, act_seqs=[777, 129], topk=130, seed=26, num_blocks=10)
-    check_full(inp, f"n_q={n_q}")
+@pytest.mark.parametrize("kv_int8", [False, True])
+@pytest.mark.parametrize("n_q", [1, 16, 50, 100])
+def test_head_counts(n_q, kv_int8):
+    # head counts that end inside a group of four lanes: Q and out move line-major
+    # through four-lane transposes that mix live and absent heads
+    inp = workloads.make_inputs(B=2, S1=1, n_q=n_q, act_seqs=[777, 129], topk=130, seed=26, num_blocks=10,
+                                kv_int8=kv_int8)
+    check_full(inp, f"n_q={n_q} int8={kv_int8}")
 
 
 def test_topk_one_and_tiny_lists():

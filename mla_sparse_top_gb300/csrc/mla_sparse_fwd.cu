@@ -639,32 +639,76 @@ __device__ __forceinline__ void copy_q_smem(const Params& p, const Ctx& c, int q
 // [0, 128) to TMEM (the lanes of the quadrant) through registers; then
 // QReady.  The heads' rows lie 1 KB apart, so the copies for shared memory
 // assign lanes to whole 128-byte lines rather than to heads (a warp-wide copy
-// then covers 4 lines, not 32); the TMEM dims are loaded per head, into the
-// registers of that head's lane.  The senders load
+// then covers 4 lines, not 32).  In the window modes the TMEM dims land the
+// same way in the warp's two staging blocks (idle between a token's last
+// partial tile and the next token's first) and are read back per head; the
+// list modes load them per head.  The senders load
 // each token's Q as soon as the previous token's score MMAs are complete, so
 // the load overlaps the softmax of that token's last tiles.
+template <int kMode>
 __device__ __forceinline__ void load_q(const Params& p, const Ctx& c, int q, int lane, int64_t qrow0, uint32_t tQ) {
   const uint8_t* qn0 = reinterpret_cast<const uint8_t*>(p.q_nope) + (qrow0 * 512 + c.crank * 256) * 2;
   const uint8_t* qr0 = reinterpret_cast<const uint8_t*>(p.q_rope) + (qrow0 * 64 + c.crank * 32) * 2;
   copy_q_smem(p, c, q, lane, qn0, qr0);
-  // dims [0, 128): this lane's head, all register loads issued before the first TMEM store
-  const bool live = q * 32 + lane < p.n_q;
-  const uint8_t* qn = qn0 + static_cast<int64_t>(lane) * 1024;
-  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  uint4 qv[16];
+  if constexpr (!lists_mode(kMode)) {
+    // Window modes (a token switch every few tiles): dims [0, 128) by
+    // line-major copies into this warp's two 4 KB staging blocks (line ch of
+    // head hh at block ch, row hh, 16-byte unit u at u ^ (hh & 7)), read back
+    // per head once the blocks' last bulk copies to the peer have read them
+    if (lane == 0) bulk_wait_read_all();
+    __syncwarp();
+    const uint32_t blk[2] = {c.sbase + kOffStaging + q * kXchgBlockBytes,
+                             c.sbase + kOffStaging + kXchgBytes + q * kXchgBlockBytes};
+    {
+      // lane: line chunk (lane / 8) % 2 and unit lane % 8 of heads 2 i + lane / 16
+      const int ch = (lane >> 3) & 1, u = lane & 7, h0 = lane >> 4;
+      const uint8_t* src = qn0 + static_cast<int64_t>(h0) * 1024 + ch * 128 + u * 16;
+      const uint32_t dst = (ch ? blk[1] : blk[0]) + h0 * 128;
 #pragma unroll
-  for (int u = 0; u < 16; ++u) qv[u] = live ? ldg16(qn + u * 16) : zero;
-#pragma unroll
-  for (int ch = 0; ch < 2; ++ch) {
-    uint32_t w[32];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      w[4 * u + 0] = qv[8 * ch + u].x;
-      w[4 * u + 1] = qv[8 * ch + u].y;
-      w[4 * u + 2] = qv[8 * ch + u].z;
-      w[4 * u + 3] = qv[8 * ch + u].w;
+      for (int i = 0; i < 16; ++i) {
+        const int hh = 2 * i + h0;
+        const bool live = q * 32 + hh < p.n_q;
+        cp_async_16(dst + i * 256 + ((u ^ (hh & 7)) << 4), live ? static_cast<const void*>(src + i * 2048) : p.q_nope,
+                    live ? 16u : 0u);
+      }
     }
-    tmem_st_32x32b_x32(tQ + 32 * ch, w);
+    cp_async_wait_all();
+    __syncwarp();  // every lane's copies have landed before any lane reads another's
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch) {
+      uint32_t w[32];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float4 v = lds16f(blk[ch] + lane * 128 + ((u ^ (lane & 7)) << 4));
+        w[4 * u + 0] = __float_as_uint(v.x);
+        w[4 * u + 1] = __float_as_uint(v.y);
+        w[4 * u + 2] = __float_as_uint(v.z);
+        w[4 * u + 3] = __float_as_uint(v.w);
+      }
+      tmem_st_32x32b_x32(tQ + 32 * ch, w);
+    }
+    __syncwarp();  // the staging blocks are read before the next partial tile is staged
+  } else {
+    // top-k lists (a switch every 32 tiles): per head into registers, which
+    // keeps the senders' per-tile code free of spills
+    const bool live = q * 32 + lane < p.n_q;
+    const uint8_t* qn = qn0 + static_cast<int64_t>(lane) * 1024;
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    uint4 qv[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) qv[u] = live ? ldg16(qn + u * 16) : zero;
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch) {
+      uint32_t w[32];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        w[4 * u + 0] = qv[8 * ch + u].x;
+        w[4 * u + 1] = qv[8 * ch + u].y;
+        w[4 * u + 2] = qv[8 * ch + u].z;
+        w[4 * u + 3] = qv[8 * ch + u].w;
+      }
+      tmem_st_32x32b_x32(tQ + 32 * ch, w);
+    }
   }
   cp_async_wait_all();
   fence_proxy_async_smem();  // cp.async data -> tensor-core reads
@@ -683,7 +727,7 @@ __device__ void sender_role(const Params& p, const Ctx& c, int q, int lane) {
   const uint32_t dst = mapa_shared(c.sbase + kOffRecv, peer);
   const uint32_t rbar0 = mapa_shared(c.bar(kBarRecvFull + 0), peer);
   const uint32_t rbar1 = mapa_shared(c.bar(kBarRecvFull + 1), peer);
-  if constexpr (!kInt8) load_q(p, c, q, lane, static_cast<int64_t>(token_of<kMode>(p, c, 0)) * p.n_q + q * 32, tQ);
+  if constexpr (!kInt8) load_q<kMode>(p, c, q, lane, static_cast<int64_t>(token_of<kMode>(p, c, 0)) * p.n_q + q * 32, tQ);
   int m = 0, m_end = seg_end<kMode>(p, c, 0);  // token ordinal and the end of its segment
   // the loop bound comes from shared memory: the two 32-column halves held in
   // registers leave none to spare for it
@@ -704,7 +748,7 @@ __device__ void sender_role(const Params& p, const Ctx& c, int q, int lane) {
       if (!warp_wait(c, kBarQFree, m & 1)) break;
       tc_fence_after();
       ++m;
-      load_q(p, c, q, lane, static_cast<int64_t>(token_of<kMode>(p, c, m)) * p.n_q + q * 32, tQ);
+      load_q<kMode>(p, c, q, lane, static_cast<int64_t>(token_of<kMode>(p, c, m)) * p.n_q + q * 32, tQ);
       m_end = seg_end<kMode>(p, c, m);
     }
   }
